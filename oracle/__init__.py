@@ -1,0 +1,243 @@
+"""CPU oracle for the fine-grained FP8 path -- TEST INFRASTRUCTURE ONLY.
+
+Thin numpy/ctypes wrapper over ``fp8q_oracle.c`` (plain C, FP64 GEMM).  Only
+``tests/``, the package's ``smoke()`` check and the benchmark's ``cpu_baseline``
+leg may import this module.  It imports nothing from the CUDA package and the
+CUDA package imports nothing from here.
+
+Each wrapper names the passage it follows; the C source carries the details.
+BF16 inputs are passed as numpy ``uint16`` bit patterns and widened exactly to
+FP32 here (a BF16 value is the upper half of an FP32 word).
+
+Parity pins: every function here is pinned by ``tests/test_oracle_*.py``
+against closed forms, invariants, brute force or an independent library
+routine -- except ``gemm_trunc_emu``'s default knobs, which the pages pin only
+loosely (one printed figure, ~2% at K=4096, inputs not stated).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+GROUP = 128
+E4M3_MAX = 448.0
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        I = ctypes.c_int
+        lib.fpo_e4m3_decode.restype = ctypes.c_double
+        lib.fpo_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.fpo_e4m3_encode.restype = ctypes.c_uint8
+        lib.fpo_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.fpo_e4m3_decode_array.argtypes = [P, I64, P]
+        lib.fpo_e4m3_encode_array.argtypes = [P, I64, P]
+        lib.fpo_tile_scale.argtypes = [ctypes.c_float, P, P]
+        for name in ("fpo_quant_1x128", "fpo_quant_128x1", "fpo_quant_128x128"):
+            getattr(lib, name).argtypes = [P, I64, I64, P, P]
+        lib.fpo_gemm_f64.argtypes = [P, P, P, P, I, I64, I64, I64, P, P, I]
+        lib.fpo_gemm_f64_entries.argtypes = [P, P, P, P, I, I64, I64, I64, P, P, I64, P, P, I]
+        lib.fpo_gemm_grouped_f64.argtypes = [P, P, P, P, P, I64, I64, I64, I64, P, P, I]
+        lib.fpo_gemm_grouped_f64_entries.argtypes = [P, P, P, P, P, I64, I64, I64, I64, P, P,
+                                                     I64, P, P, I]
+        lib.fpo_gemm_exact_int.argtypes = [P, P, P, P, I, I64, I64, I64, P, I]
+        lib.fpo_gemm_trunc_emu.argtypes = [P, P, P, P, I, I64, I64, I64, I64, I, I, I, P, I]
+        lib.fpo_gemm_f64_prefix.argtypes = [P, P, P, P, I, I64, I64, I64, I64, P, I]
+        lib.fpo_max_threads.restype = I
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def max_threads() -> int:
+    return int(_load().fpo_max_threads())
+
+
+def widen(x) -> np.ndarray:
+    """FP32 view of an input: float arrays pass through, uint16 is read as BF16 bits."""
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        return (x.astype(np.uint32) << 16).view(np.float32)
+    return _c(x, np.float32)
+
+
+# ------------------------------------------------------------------ codec
+def e4m3_decode(b) -> np.ndarray:
+    """E4M3 byte -> value (FP64), OCP definition; "unified E4M3 format"."""
+    b = _c(b, np.uint8)
+    out = np.empty(b.shape, np.float64)
+    _load().fpo_e4m3_decode_array(_ptr(b), b.size, _ptr(out))
+    return out
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """FP32 -> E4M3 byte, round-to-nearest-even, saturating at +-448, NaN -> 0x7F."""
+    v = _c(v, np.float32)
+    out = np.empty(v.shape, np.uint8)
+    _load().fpo_e4m3_encode_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def tile_scale(amax: float):
+    """(s, inv) for one tile: s = fl32(amax/448), inv = fl32(448/amax)."""
+    s = ctypes.c_float()
+    inv = ctypes.c_float()
+    _load().fpo_tile_scale(ctypes.c_float(amax), ctypes.byref(s), ctypes.byref(inv))
+    return np.float32(s.value), np.float32(inv.value)
+
+
+# ------------------------------------------------------------- quantizers
+def _nb(n):
+    return (n + GROUP - 1) // GROUP
+
+
+def quant_1x128(x):
+    """Per token per 128 channels ("Six Reasons...", para. 3).  x[M][K] ->
+    q[M][K] uint8, s[ceil(K/128)][M] float32."""
+    x = widen(x)
+    M, K = x.shape
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((_nb(K), M), np.float32)
+    _load().fpo_quant_1x128(_ptr(x), M, K, _ptr(q), _ptr(s))
+    return q, s
+
+
+def quant_128x1(x):
+    """Per 128 tokens per channel, written transposed ("Six Reasons...", para. 3).
+    x[T][C] -> qT[C][T] uint8, sT[ceil(T/128)][C] float32."""
+    x = widen(x)
+    T, C = x.shape
+    q = np.empty((C, T), np.uint8)
+    s = np.empty((_nb(T), C), np.float32)
+    _load().fpo_quant_128x1(_ptr(x), T, C, _ptr(q), _ptr(s))
+    return q, s
+
+
+def quant_128x128(w):
+    """Per 128x128 weight block ("Six Reasons...", para. 3).  w[N][K] ->
+    q[N][K] uint8, s[ceil(N/128)][ceil(K/128)] float32."""
+    w = widen(w)
+    N, K = w.shape
+    q = np.empty((N, K), np.uint8)
+    s = np.empty((_nb(N), _nb(K)), np.float32)
+    _load().fpo_quant_128x128(_ptr(w), N, K, _ptr(q), _ptr(s))
+    return q, s
+
+
+# ------------------------------------------------------------------- GEMM
+BSCALE_BLOCK128 = 0
+BSCALE_ROW1x128 = 1
+
+
+def gemm(A8, sA, B8, sB, bmode=BSCALE_BLOCK128, threads=0):
+    """C = dequant(A8) @ dequant(B8)^T in FP64, plus sum_k |a_k b_k| per entry."""
+    A8, B8 = _c(A8, np.uint8), _c(B8, np.uint8)
+    sA, sB = _c(sA, np.float32), _c(sB, np.float32)
+    M, K = A8.shape
+    N = B8.shape[0]
+    C = np.empty((M, N), np.float64)
+    Cabs = np.empty((M, N), np.float64)
+    _load().fpo_gemm_f64(_ptr(A8), _ptr(sA), _ptr(B8), _ptr(sB), bmode, M, N, K,
+                         _ptr(C), _ptr(Cabs), threads)
+    return C, Cabs
+
+
+def gemm_entries(A8, sA, B8, sB, mi, ni, bmode=BSCALE_BLOCK128, threads=0):
+    """The same GEMM evaluated only at entries (mi[i], ni[i])."""
+    A8, B8 = _c(A8, np.uint8), _c(B8, np.uint8)
+    sA, sB = _c(sA, np.float32), _c(sB, np.float32)
+    mi, ni = _c(mi, np.int64), _c(ni, np.int64)
+    M, K = A8.shape
+    N = B8.shape[0]
+    C = np.empty(mi.shape, np.float64)
+    Cabs = np.empty(mi.shape, np.float64)
+    _load().fpo_gemm_f64_entries(_ptr(A8), _ptr(sA), _ptr(B8), _ptr(sB), bmode, M, N, K,
+                                 _ptr(mi), _ptr(ni), mi.size, _ptr(C), _ptr(Cabs), threads)
+    return C, Cabs
+
+
+def gemm_grouped(A8, sA, B8, sB, m_offsets, threads=0):
+    """MoE grouped GEMM ([P4] item 8): group e's rows times its own B8[e]."""
+    A8, B8 = _c(A8, np.uint8), _c(B8, np.uint8)
+    sA, sB = _c(sA, np.float32), _c(sB, np.float32)
+    mo = _c(m_offsets, np.int64)
+    Mtot, K = A8.shape
+    G, N, _ = B8.shape
+    C = np.zeros((Mtot, N), np.float64)
+    Cabs = np.zeros((Mtot, N), np.float64)
+    _load().fpo_gemm_grouped_f64(_ptr(A8), _ptr(sA), _ptr(B8), _ptr(sB), _ptr(mo), G, Mtot, N,
+                                 K, _ptr(C), _ptr(Cabs), threads)
+    return C, Cabs
+
+
+def gemm_grouped_entries(A8, sA, B8, sB, m_offsets, mi, ni, threads=0):
+    A8, B8 = _c(A8, np.uint8), _c(B8, np.uint8)
+    sA, sB = _c(sA, np.float32), _c(sB, np.float32)
+    mo = _c(m_offsets, np.int64)
+    mi, ni = _c(mi, np.int64), _c(ni, np.int64)
+    Mtot, K = A8.shape
+    G, N, _ = B8.shape
+    C = np.empty(mi.shape, np.float64)
+    Cabs = np.empty(mi.shape, np.float64)
+    _load().fpo_gemm_grouped_f64_entries(_ptr(A8), _ptr(sA), _ptr(B8), _ptr(sB), _ptr(mo), G,
+                                         Mtot, N, K, _ptr(mi), _ptr(ni), mi.size, _ptr(C),
+                                         _ptr(Cabs), threads)
+    return C, Cabs
+
+
+def gemm_exact_int(A8, sA, B8, sB, bmode=BSCALE_BLOCK128, threads=0):
+    """Independent route: exact int64 group sums, then FP64 scaling."""
+    A8, B8 = _c(A8, np.uint8), _c(B8, np.uint8)
+    sA, sB = _c(sA, np.float32), _c(sB, np.float32)
+    M, K = A8.shape
+    N = B8.shape[0]
+    C = np.empty((M, N), np.float64)
+    _load().fpo_gemm_exact_int(_ptr(A8), _ptr(sA), _ptr(B8), _ptr(sB), bmode, M, N, K,
+                               _ptr(C), threads)
+    return C
+
+
+def gemm_trunc_emu(A8, sA, B8, sB, kmax=None, chunk=4, mbits=13, promote=0,
+                   bmode=BSCALE_BLOCK128, threads=0):
+    """Limited-precision accumulation stand-in ("Six Reasons...", paras. 2-3).
+
+    promote=0: no promotion over the first kmax elements of K.
+    promote=P: the limited accumulator restarts every P elements and partials
+    are summed in FP64 (promotion)."""
+    A8, B8 = _c(A8, np.uint8), _c(B8, np.uint8)
+    sA, sB = _c(sA, np.float32), _c(sB, np.float32)
+    M, K = A8.shape
+    N = B8.shape[0]
+    kmax = K if kmax is None else int(kmax)
+    C = np.empty((M, N), np.float64)
+    _load().fpo_gemm_trunc_emu(_ptr(A8), _ptr(sA), _ptr(B8), _ptr(sB), bmode, M, N, K, kmax,
+                               chunk, mbits, promote, _ptr(C), threads)
+    return C
+
+
+def gemm_prefix(A8, sA, B8, sB, kmax, bmode=BSCALE_BLOCK128, threads=0):
+    """FP64 GEMM over the first kmax elements of K (for the emulator's error)."""
+    A8, B8 = _c(A8, np.uint8), _c(B8, np.uint8)
+    sA, sB = _c(sA, np.float32), _c(sB, np.float32)
+    M, K = A8.shape
+    N = B8.shape[0]
+    C = np.empty((M, N), np.float64)
+    _load().fpo_gemm_f64_prefix(_ptr(A8), _ptr(sA), _ptr(B8), _ptr(sB), bmode, M, N, K,
+                                int(kmax), _ptr(C), threads)
+    return C
