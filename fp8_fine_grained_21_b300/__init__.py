@@ -1,0 +1,228 @@
+"""fp8q: fine-grained FP8 (E4M3) quantization and block-scaled FP8 GEMM on B300.
+
+Thin ctypes binding over ``libfp8q.so`` (C ABI in ``include/fp8q.h``).  The
+functions named ``fp8q_*`` mirror the C entry points one to one and take torch
+CUDA tensors for every buffer; the short-named helpers allocate the outputs
+with torch and call them.  Torch supplies device memory and streams only:
+every step of the computation runs in the library's CUDA kernels.  There is no
+CPU fallback -- if the library is missing or a tensor is not on a CUDA device,
+the call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "Fp8qError", "library_path", "load",
+    "fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128",
+    "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_get_device_status",
+    "fp8q_status_string", "fp8q_version",
+    "quant_act_1x128", "quant_act_128x1", "quant_w_128x128", "gemm", "gemm_grouped",
+    "F32", "BF16", "BSCALE_BLOCK128", "BSCALE_ROW1x128",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(HERE, "libfp8q.so")
+
+F32, BF16 = 0, 1
+BSCALE_BLOCK128, BSCALE_ROW1x128 = 0, 1
+STATUS_NAMES = {0: "FP8Q_OK", 1: "FP8Q_ERR_INVALID_ARG", 2: "FP8Q_ERR_UNSUPPORTED_SHAPE",
+                3: "FP8Q_ERR_MISALIGNED", 4: "FP8Q_ERR_CUDA", 5: "FP8Q_ERR_TIMEOUT",
+                6: "FP8Q_ERR_BAD_GROUPS"}
+EXPORTS = ("fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128", "fp8q_gemm",
+           "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_get_device_status", "fp8q_status_string",
+           "fp8q_version")
+
+
+class Fp8qError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %s (%d)" % (fn, STATUS_NAMES.get(status, "?"), status))
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libfp8q.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError("fp8q CUDA library not built (%s missing); run "
+                           "`python -m fp8_fine_grained_21_b300.build`" % _LIB_PATH)
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    for name in ("fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128"):
+        f = getattr(lib, name)
+        f.argtypes = [P, I, I64, I64, P, P, P]
+        f.restype = I
+    lib.fp8q_gemm.argtypes = [P, P, P, P, P, I64, I64, I64, I]
+    lib.fp8q_gemm.restype = I
+    lib.fp8q_gemm_ex.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, P]
+    lib.fp8q_gemm_ex.restype = I
+    lib.fp8q_gemm_grouped.argtypes = [P, P, P, P, P, P, I, I64, I64, I64, I, P]
+    lib.fp8q_gemm_grouped.restype = I
+    lib.fp8q_get_device_status.argtypes = [P]
+    lib.fp8q_get_device_status.restype = I
+    lib.fp8q_status_string.argtypes = [I]
+    lib.fp8q_status_string.restype = ctypes.c_char_p
+    lib.fp8q_version.argtypes = []
+    lib.fp8q_version.restype = I
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------- marshalling
+_IN_DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> ctypes.c_void_p:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (no CPU path)" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise Fp8qError(fn, rc)
+
+
+def _in_dtype(x):
+    try:
+        return _IN_DTYPES[x.dtype]
+    except KeyError:
+        raise ValueError("input must be float32 or bfloat16, got %s" % x.dtype) from None
+
+
+def _out_dtype(dt):
+    if dt == torch.float32:
+        return F32
+    if dt == torch.bfloat16:
+        return BF16
+    raise ValueError("output must be float32 or bfloat16, got %s" % dt)
+
+
+# ------------------------------------------------------- same-name bindings
+def fp8q_quant_act_1x128(x, q, s, stream=None):
+    M, K = x.shape
+    _check("fp8q_quant_act_1x128", load().fp8q_quant_act_1x128(
+        _dev(x, "x"), _in_dtype(x), M, K, _dev(q, "q", torch.uint8),
+        _dev(s, "s", torch.float32), _stream(stream)))
+
+
+def fp8q_quant_act_128x1(x, qT, sT, stream=None):
+    T, C = x.shape
+    _check("fp8q_quant_act_128x1", load().fp8q_quant_act_128x1(
+        _dev(x, "x"), _in_dtype(x), T, C, _dev(qT, "qT", torch.uint8),
+        _dev(sT, "sT", torch.float32), _stream(stream)))
+
+
+def fp8q_quant_w_128x128(w, q, s, stream=None):
+    N, K = w.shape
+    _check("fp8q_quant_w_128x128", load().fp8q_quant_w_128x128(
+        _dev(w, "w"), _in_dtype(w), N, K, _dev(q, "q", torch.uint8),
+        _dev(s, "s", torch.float32), _stream(stream)))
+
+
+def fp8q_gemm(A8, sA, B8, sB, C):
+    M, K = A8.shape
+    N = B8.shape[0]
+    _check("fp8q_gemm", load().fp8q_gemm(
+        _dev(A8, "A8", torch.uint8), _dev(sA, "sA", torch.float32), _dev(B8, "B8", torch.uint8),
+        _dev(sB, "sB", torch.float32), _dev(C, "C"), M, N, K, _out_dtype(C.dtype)))
+
+
+def fp8q_gemm_ex(A8, sA, B8, sB, C, bscale=BSCALE_BLOCK128, stream=None):
+    M, K = A8.shape
+    N = B8.shape[0]
+    _check("fp8q_gemm_ex", load().fp8q_gemm_ex(
+        _dev(A8, "A8", torch.uint8), _dev(sA, "sA", torch.float32), _dev(B8, "B8", torch.uint8),
+        _dev(sB, "sB", torch.float32), _dev(C, "C"), M, N, K, _out_dtype(C.dtype), int(bscale),
+        _stream(stream)))
+
+
+def fp8q_gemm_grouped(A8, sA, B8, sB, C, m_offsets, stream=None):
+    Mtot, K = A8.shape
+    G, N, _ = B8.shape
+    _check("fp8q_gemm_grouped", load().fp8q_gemm_grouped(
+        _dev(A8, "A8", torch.uint8), _dev(sA, "sA", torch.float32), _dev(B8, "B8", torch.uint8),
+        _dev(sB, "sB", torch.float32), _dev(C, "C"), _dev(m_offsets, "m_offsets", torch.int32),
+        G, Mtot, N, K, _out_dtype(C.dtype), _stream(stream)))
+
+
+def fp8q_get_device_status(stream=None) -> int:
+    return int(load().fp8q_get_device_status(_stream(stream)))
+
+
+def fp8q_status_string(status: int) -> str:
+    return load().fp8q_status_string(int(status)).decode()
+
+
+def fp8q_version() -> int:
+    return int(load().fp8q_version())
+
+
+# -------------------------------------------------------- allocating helpers
+def _scales(n):
+    return (n + 127) // 128
+
+
+def quant_act_1x128(x, stream=None):
+    """x[M][K] -> (q[M][K] uint8 E4M3, s[K/128][M] float32)."""
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    s = torch.empty((_scales(K), M), dtype=torch.float32, device=x.device)
+    fp8q_quant_act_1x128(x, q, s, stream)
+    return q, s
+
+
+def quant_act_128x1(x, stream=None):
+    """x[T][C] -> (qT[C][T] uint8, sT[T/128][C] float32)."""
+    T, C = x.shape
+    q = torch.empty((C, T), dtype=torch.uint8, device=x.device)
+    s = torch.empty((_scales(T), C), dtype=torch.float32, device=x.device)
+    fp8q_quant_act_128x1(x, q, s, stream)
+    return q, s
+
+
+def quant_w_128x128(w, stream=None):
+    """w[N][K] -> (q[N][K] uint8, s[N/128][K/128] float32)."""
+    N, K = w.shape
+    q = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    s = torch.empty((_scales(N), _scales(K)), dtype=torch.float32, device=w.device)
+    fp8q_quant_w_128x128(w, q, s, stream)
+    return q, s
+
+
+def gemm(A8, sA, B8, sB, out_dtype=torch.bfloat16, bscale=BSCALE_BLOCK128, stream=None):
+    """C[M][N] = dequant(A8) @ dequant(B8)^T."""
+    C = torch.empty((A8.shape[0], B8.shape[0]), dtype=out_dtype, device=A8.device)
+    fp8q_gemm_ex(A8, sA, B8, sB, C, bscale, stream)
+    return C
+
+
+def gemm_grouped(A8, sA, B8, sB, m_offsets, out_dtype=torch.bfloat16, stream=None):
+    """Grouped GEMM; rows outside every group are left unwritten (uninitialized)."""
+    C = torch.empty((A8.shape[0], B8.shape[1]), dtype=out_dtype, device=A8.device)
+    fp8q_gemm_grouped(A8, sA, B8, sB, C, m_offsets, stream)
+    return C

@@ -1,0 +1,271 @@
+// C ABI of the fp8q library (declared in include/fp8q.h): argument checks,
+// TMA descriptor encoding and kernel launches.  No allocation happens here:
+// every buffer belongs to the caller; the only library state is a per-device
+// status word (a static __device__ variable) and cached launch attributes.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fp8q.h"
+#include "gemm.cuh"
+#include "quant.cuh"
+
+namespace fp8q {
+
+__device__ int g_status;   // sticky device-side status, one per device
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    int* status = nullptr;            // device address of g_status on this device
+    bool gemm_attr[2][2][2] = {};     // dynamic-smem attribute set, per kernel instance
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int cuda_fail() {
+    cudaGetLastError();   // clear the sticky runtime error of this thread
+    return FP8Q_ERR_CUDA;
+}
+
+// Per-device set-up on first use: SM count and the address of g_status.
+int device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail();
+    if (dev < 0 || dev >= kMaxDevices) return FP8Q_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cuda_fail();
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return cuda_fail();
+        d.status = static_cast<int*>(p);
+        if (!g_encode) {
+            cudaDriverEntryPointQueryResult q;
+            void* fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return cuda_fail();
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return FP8Q_OK;
+}
+
+// 2-D uint8 tensor [rows][K], K-major, boxes of 128 (K) x box_rows with
+// 128-byte swizzle (one box row = one swizzle row).
+int encode_kmajor(CUtensorMap* map, const uint8_t* base, int64_t K, int64_t rows, int box_rows) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+template <int BN, bool kRowB, bool kBf16>
+int launch_gemm_inst(DeviceState* d, const CUtensorMap& ta, const CUtensorMap& tb,
+                     const GemmArgs& args, int tiles_upper, cudaStream_t st) {
+    using S = GemmShape<BN>;
+    auto kern = k_gemm<BN, kRowB, kBf16>;
+    bool& attr = d->gemm_attr[BN == 256][kRowB][kBf16];
+    if (!attr) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 S::kSmemBytes) != cudaSuccess)
+            return cuda_fail();
+        attr = true;
+    }
+    int grid = tiles_upper < d->num_sms ? tiles_upper : d->num_sms;
+    if (grid < 1) grid = 1;
+    kern<<<grid, S::kThreads, S::kSmemBytes, st>>>(ta, tb, args);
+    return cudaGetLastError() == cudaSuccess ? FP8Q_OK : cuda_fail();
+}
+
+template <int BN>
+int launch_gemm_bn(DeviceState* d, const CUtensorMap& ta, const CUtensorMap& tb,
+                   const GemmArgs& args, int tiles_upper, bool row_b, bool bf16, cudaStream_t st) {
+    if (row_b)
+        return bf16 ? launch_gemm_inst<BN, true, true>(d, ta, tb, args, tiles_upper, st)
+                    : launch_gemm_inst<BN, true, false>(d, ta, tb, args, tiles_upper, st);
+    return bf16 ? launch_gemm_inst<BN, false, true>(d, ta, tb, args, tiles_upper, st)
+                : launch_gemm_inst<BN, false, false>(d, ta, tb, args, tiles_upper, st);
+}
+
+int gemm_common(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB, void* C,
+                const int* m_offsets, int G, int64_t M, int64_t N, int64_t K, int out_dtype,
+                int bscale, cudaStream_t st) {
+    if (!A8 || !sA || !B8 || !sB || !C) return FP8Q_ERR_INVALID_ARG;
+    if (out_dtype != FP8Q_F32 && out_dtype != FP8Q_BF16) return FP8Q_ERR_INVALID_ARG;
+    if (bscale != FP8Q_BSCALE_BLOCK128 && bscale != FP8Q_BSCALE_ROW1x128) return FP8Q_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0) return FP8Q_ERR_INVALID_ARG;
+    if (M % 128 || N % 128 || K % 128) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (M > (int64_t(1) << 30) || N > (int64_t(1) << 24) || K > (int64_t(1) << 30))
+        return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (int64_t(G) * N > (int64_t(1) << 31) - 1) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(A8, 16) || !aligned(B8, 16) || !aligned(sA, 16) || !aligned(C, 16))
+        return FP8Q_ERR_MISALIGNED;
+    if (!aligned(sB, bscale == FP8Q_BSCALE_ROW1x128 ? 16 : 4)) return FP8Q_ERR_MISALIGNED;
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != FP8Q_OK) return rc;
+    const int BN = (N % 256 == 0) ? 256 : 128;
+    CUtensorMap ta, tb;
+    std::memset(&ta, 0, sizeof(ta));
+    std::memset(&tb, 0, sizeof(tb));
+    if ((rc = encode_kmajor(&ta, A8, K, M, 128)) != FP8Q_OK) return rc;
+    if ((rc = encode_kmajor(&tb, B8, K, int64_t(G) * N, BN)) != FP8Q_OK) return rc;
+    GemmArgs args;
+    args.sA = sA;
+    args.sB = sB;
+    args.C = C;
+    args.m_offsets = m_offsets;
+    args.M_total = static_cast<int>(M);
+    args.N = static_cast<int>(N);
+    args.K = static_cast<int>(K);
+    args.G = G;
+    args.status = d->status;
+    const int64_t tiles = (M / 128) * (N / BN);
+    const int tiles_upper = tiles > (int64_t(1) << 30) ? (1 << 30) : static_cast<int>(tiles);
+    const bool row_b = bscale == FP8Q_BSCALE_ROW1x128;
+    const bool bf16 = out_dtype == FP8Q_BF16;
+    return BN == 256 ? launch_gemm_bn<256>(d, ta, tb, args, tiles_upper, row_b, bf16, st)
+                     : launch_gemm_bn<128>(d, ta, tb, args, tiles_upper, row_b, bf16, st);
+}
+
+int check_in_dtype(int t) { return (t == FP8Q_F32 || t == FP8Q_BF16) ? FP8Q_OK : FP8Q_ERR_INVALID_ARG; }
+
+int launched() { return cudaGetLastError() == cudaSuccess ? FP8Q_OK : cuda_fail(); }
+
+}  // namespace
+}  // namespace fp8q
+
+using namespace fp8q;
+
+extern "C" {
+
+int fp8q_quant_act_1x128(const void* x, int in_dtype, int64_t M, int64_t K, uint8_t* q, float* s,
+                         fp8q_stream_t stream) {
+    if (!x || !q || !s) return FP8Q_ERR_INVALID_ARG;
+    if (check_in_dtype(in_dtype) != FP8Q_OK || M <= 0 || K <= 0) return FP8Q_ERR_INVALID_ARG;
+    if (K % 128) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    const int64_t yblocks = (M + kQ1Rows - 1) / kQ1Rows;
+    if (yblocks > 65535 || K / 128 > 0x7fffffff) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(x, 16) || !aligned(q, 16) || !aligned(s, 4)) return FP8Q_ERR_MISALIGNED;
+    const dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(yblocks));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (in_dtype == FP8Q_BF16)
+        k_quant_1x128<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), M,
+                                                           K, q, s);
+    else
+        k_quant_1x128<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), M, K, q, s);
+    return launched();
+}
+
+int fp8q_quant_act_128x1(const void* x, int in_dtype, int64_t T, int64_t C, uint8_t* qT, float* sT,
+                         fp8q_stream_t stream) {
+    if (!x || !qT || !sT) return FP8Q_ERR_INVALID_ARG;
+    if (check_in_dtype(in_dtype) != FP8Q_OK || T <= 0 || C <= 0) return FP8Q_ERR_INVALID_ARG;
+    if (T % 128 || C % 64) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (T / 128 > 65535 || C / 64 > 0x7fffffff) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(x, 16) || !aligned(qT, 16) || !aligned(sT, 4)) return FP8Q_ERR_MISALIGNED;
+    const dim3 grid(static_cast<unsigned>(C / 64), static_cast<unsigned>(T / 128));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (in_dtype == FP8Q_BF16)
+        k_quant_128x1<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), T,
+                                                           C, qT, sT);
+    else
+        k_quant_128x1<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), T, C, qT, sT);
+    return launched();
+}
+
+int fp8q_quant_w_128x128(const void* w, int in_dtype, int64_t N, int64_t K, uint8_t* q, float* s,
+                         fp8q_stream_t stream) {
+    if (!w || !q || !s) return FP8Q_ERR_INVALID_ARG;
+    if (check_in_dtype(in_dtype) != FP8Q_OK || N <= 0 || K <= 0) return FP8Q_ERR_INVALID_ARG;
+    if (N % 128 || K % 128) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (N / 128 > 65535 || K / 128 > 0x7fffffff) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(w, 16) || !aligned(q, 16) || !aligned(s, 4)) return FP8Q_ERR_MISALIGNED;
+    const dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (in_dtype == FP8Q_BF16)
+        k_quant_128x128<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w), N,
+                                                             K, q, s);
+    else
+        k_quant_128x128<float><<<grid, 256, 0, st>>>(static_cast<const float*>(w), N, K, q, s);
+    return launched();
+}
+
+int fp8q_gemm(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB, void* C,
+              int64_t M, int64_t N, int64_t K, int out_dtype) {
+    return gemm_common(A8, sA, B8, sB, C, nullptr, 1, M, N, K, out_dtype, FP8Q_BSCALE_BLOCK128,
+                       nullptr);
+}
+
+int fp8q_gemm_ex(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB, void* C,
+                 int64_t M, int64_t N, int64_t K, int out_dtype, int bscale, fp8q_stream_t stream) {
+    return gemm_common(A8, sA, B8, sB, C, nullptr, 1, M, N, K, out_dtype, bscale,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8q_gemm_grouped(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,
+                      void* C, const int* m_offsets, int G, int64_t M_total, int64_t N, int64_t K,
+                      int out_dtype, fp8q_stream_t stream) {
+    if (!m_offsets) return FP8Q_ERR_INVALID_ARG;
+    if (G < 1 || G > kMaxGroups) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(m_offsets, 4)) return FP8Q_ERR_MISALIGNED;
+    return gemm_common(A8, sA, B8, sB, C, m_offsets, G, M_total, N, K, out_dtype,
+                       FP8Q_BSCALE_BLOCK128, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8q_get_device_status(fp8q_stream_t stream) {
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != FP8Q_OK) return rc;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return cuda_fail();
+    int v = 0;
+    if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return cuda_fail();
+    if (v != FP8Q_OK) {
+        const int zero = 0;
+        if (cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return cuda_fail();
+    }
+    return v;
+}
+
+const char* fp8q_status_string(int status) {
+    switch (status) {
+        case FP8Q_OK: return "ok";
+        case FP8Q_ERR_INVALID_ARG: return "invalid argument";
+        case FP8Q_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case FP8Q_ERR_MISALIGNED: return "misaligned pointer";
+        case FP8Q_ERR_CUDA: return "CUDA error";
+        case FP8Q_ERR_TIMEOUT: return "device pipeline wait timed out";
+        case FP8Q_ERR_BAD_GROUPS: return "invalid group offsets";
+        default: return "unknown status";
+    }
+}
+
+int fp8q_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,160 @@
+/*
+ * fp8q -- fine-grained FP8 (E4M3) quantization and block-scaled FP8 GEMM
+ * for NVIDIA B300 (sm_103a).  C ABI.
+ *
+ * The operations follow DeepSeek-V3's FP8 training recipe as described on the
+ * pages:
+ *   "Six Reasons Deepseek Ai Is A Waste Of Time" (myomija.com), paras. 1-4;
+ *   codingmall.com knowledge-base article on FP8 in DeepSeek-V3 (Greek),
+ *     sections "fine-grained quantization", "online quantization",
+ *     "increased accumulation precision", "unified E4M3 format";
+ *   codingmall.com article on FP8 GEMM in DeepSeek-V3 (Japanese), items 1-8.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All data pointers are DEVICE pointers owned by the caller; the library
+ *   never allocates, frees or keeps them.  Every call is asynchronous on the
+ *   given stream (a cudaStream_t; NULL = the legacy default stream) and does
+ *   not synchronize.
+ * - Return value: FP8Q_OK or an fp8q_status error code.  Arguments are
+ *   checked before anything is launched; on error nothing is launched and
+ *   the outputs are untouched.  A failed launch returns FP8Q_ERR_CUDA.
+ * - Device-side problems (an inconsistent m_offsets array, a pipeline wait
+ *   that exceeded its time limit) are recorded in a sticky device status word
+ *   and read with fp8q_get_device_status().  Kernels never trap.
+ * - FP8 data is E4M3 (OCP: bias 7, no infinities, 0x7F/0xFF = NaN, largest
+ *   finite value 448) stored one byte per element.  The cast is
+ *   round-to-nearest-even with saturation to +-448; the sign of zero is kept.
+ * - Online scaling ("online quantization" section; para. 1 of "Six
+ *   Reasons..."): per group, amax = max |x| over the group;
+ *   s = fl32(amax / 448) is stored; each element is cast from
+ *   fl32(x * fl32(448 / amax)).  A group with amax == 0 stores s = 1.
+ *   448/amax overflowing FP32 is clamped to FLT_MAX.  Dequantized value =
+ *   decode(q) * s.  Inputs must be finite.
+ * - Row-major, last index contiguous.  Sizes are element counts.
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8Q_API __attribute__((visibility("default")))
+#else
+#define FP8Q_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* fp8q_stream_t;
+
+typedef enum {
+    FP8Q_OK = 0,
+    FP8Q_ERR_INVALID_ARG = 1,      /* null pointer, non-positive size, bad enum */
+    FP8Q_ERR_UNSUPPORTED_SHAPE = 2,/* a size this version does not tile (see each call) */
+    FP8Q_ERR_MISALIGNED = 3,       /* a pointer is not 16-byte aligned */
+    FP8Q_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed */
+    FP8Q_ERR_TIMEOUT = 5,          /* device: a pipeline wait exceeded its limit */
+    FP8Q_ERR_BAD_GROUPS = 6        /* device: m_offsets not monotone / not multiples of 128 /
+                                      beyond M_total */
+} fp8q_status;
+
+typedef enum { FP8Q_F32 = 0, FP8Q_BF16 = 1 } fp8q_dtype;
+
+/* How the B operand's scales are grouped (see fp8q_gemm_ex). */
+typedef enum {
+    FP8Q_BSCALE_BLOCK128 = 0,      /* 128x128 weight blocks: sB[N/128][K/128] */
+    FP8Q_BSCALE_ROW1x128 = 1       /* 1x128 tiles of B's rows: sB[K/128][N] */
+} fp8q_bscale;
+
+/* ---------------------------------------------------------------- quantize */
+
+/* Activations, one scale per 1x128 tile (per token per 128 channels):
+ * "Six Reasons...", para. 3 (grouping item 1); "fine-grained quantization".
+ *   x   [M][K]  in_dtype (FP8Q_F32 or FP8Q_BF16), 16-byte aligned
+ *   q   [M][K]  uint8 E4M3, 16-byte aligned
+ *   s   [K/128][M] float32 (scale of row m, group g at s[g*M + m]), 4-byte aligned
+ * Requires M >= 1, K a multiple of 128. */
+FP8Q_API int fp8q_quant_act_1x128(const void* x, int in_dtype, int64_t M, int64_t K,
+                         uint8_t* q, float* s, fp8q_stream_t stream);
+
+/* Activations regrouped for the backward pass, one scale per 128x1 tile
+ * (128 consecutive tokens of one channel), written transposed so that the
+ * result is a K-major GEMM operand whose K runs over tokens:
+ * "Six Reasons...", para. 3 (1x128 -> 128x1 conversion in the backward pass).
+ *   x   [T][C]  in_dtype, 16-byte aligned
+ *   qT  [C][T]  uint8 E4M3, 16-byte aligned
+ *   sT  [T/128][C] float32 (scale of channel c, token group tb at sT[tb*C + c])
+ * Requires T a multiple of 128, C a multiple of 64. */
+FP8Q_API int fp8q_quant_act_128x1(const void* x, int in_dtype, int64_t T, int64_t C,
+                         uint8_t* qT, float* sT, fp8q_stream_t stream);
+
+/* Weights, one scale per 128x128 block (128 output x 128 input channels):
+ * "Six Reasons...", para. 3 (grouping item 2); "fine-grained quantization".
+ *   w   [N][K]  in_dtype, 16-byte aligned
+ *   q   [N][K]  uint8 E4M3, 16-byte aligned
+ *   s   [N/128][K/128] float32
+ * Requires N and K multiples of 128. */
+FP8Q_API int fp8q_quant_w_128x128(const void* w, int in_dtype, int64_t N, int64_t K,
+                         uint8_t* q, float* s, fp8q_stream_t stream);
+
+/* -------------------------------------------------------------------- GEMM */
+
+/* Block-scaled FP8 GEMM  C[M][N] = sum_k (A8[m][k] sA) (B8[n][k] sB), i.e.
+ * C = A * B^T with both operands K-major:  "Six Reasons...", paras. 1-2 (FP8
+ * inputs, BF16/FP32 outputs, per-group scaling factors along K applied as
+ * dequantization on the CUDA cores) and para. 3 / "increased accumulation
+ * precision" (tensor-core partials of each 128-element K block are promoted
+ * to FP32 registers, scaled, and accumulated in full FP32).
+ *   A8  [M][K]  uint8 E4M3, 16-byte aligned     sA [K/128][M] float32, 16-byte aligned
+ *   B8  [N][K]  uint8 E4M3, 16-byte aligned     sB [N/128][K/128] float32
+ *   C   [M][N]  out_dtype (FP8Q_F32 or FP8Q_BF16, BF16 rounded to nearest even),
+ *               16-byte aligned; fully overwritten.
+ * Requires M, N, K multiples of 128.  Runs on the legacy default stream. */
+FP8Q_API int fp8q_gemm(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,
+              void* C, int64_t M, int64_t N, int64_t K, int out_dtype);
+
+/* fp8q_gemm with a stream and a choice of B-scale grouping.
+ * bscale = FP8Q_BSCALE_ROW1x128 is the weight-gradient form
+ * dW = dY^T X: both operands come from fp8q_quant_act_128x1 (K runs over
+ * tokens) and the scale of output (m, n) in K group g is sA[g][m] * sB[g][n];
+ * sB is [K/128][N] and must be 16-byte aligned. */
+FP8Q_API int fp8q_gemm_ex(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,
+                 void* C, int64_t M, int64_t N, int64_t K, int out_dtype, int bscale,
+                 fp8q_stream_t stream);
+
+/* Grouped (MoE) GEMM: "codingmall ... FP8 GEMM" item 8 (dense and MoE
+ * support).  Group e owns rows [m_offsets[e], m_offsets[e+1]) of A8 and C and
+ * multiplies them by its own weights:
+ *   A8  [M_total][K]      sA [K/128][M_total]
+ *   B8  [G][N][K]         sB [G][N/128][K/128]
+ *   C   [M_total][N]      rows outside every group are not written
+ *   m_offsets  DEVICE int32 array of G+1 entries, non-decreasing, each
+ *              a multiple of 128, m_offsets[G] <= M_total; checked on the
+ *              device (FP8Q_ERR_BAD_GROUPS via fp8q_get_device_status, and
+ *              then nothing is written).
+ * Requires 1 <= G <= 512, M_total, N, K multiples of 128.  Block scales only. */
+FP8Q_API int fp8q_gemm_grouped(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,
+                      void* C, const int* m_offsets, int G, int64_t M_total, int64_t N,
+                      int64_t K, int out_dtype, fp8q_stream_t stream);
+
+/* ------------------------------------------------------------------ status */
+
+/* Synchronizes `stream`, returns the sticky device status of the current
+ * device (FP8Q_OK if no kernel recorded a problem) and clears it. */
+FP8Q_API int fp8q_get_device_status(fp8q_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+FP8Q_API const char* fp8q_status_string(int status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+FP8Q_API int fp8q_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */

@@ -1,0 +1,104 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+entry point the header declares, and rejects bad arguments on the host
+before touching the device (nothing here launches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8q.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_fine_grained_21_b300 import build as b
+
+    b.build()
+    import fp8_fine_grained_21_b300 as fq
+
+    return fq.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"FP8Q_API\s+[\w\s\*]+?\b(fp8q_\w+)\s*\(", text)
+
+
+def test_header_declares_expected_calls():
+    names = set(declared_functions())
+    for n in ("fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128",
+              "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_get_device_status",
+              "fp8q_status_string", "fp8q_version"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_binding_names_match_header():
+    import fp8_fine_grained_21_b300 as fq
+
+    for n in declared_functions():
+        assert callable(getattr(fq, n)), n
+
+
+def test_status_strings_and_version(lib):
+    assert lib.fp8q_status_string(0) == b"ok"
+    assert lib.fp8q_status_string(5) == b"device pipeline wait timed out"
+    assert lib.fp8q_status_string(99) == b"unknown status"
+    assert lib.fp8q_version() == 100
+
+
+P = ctypes.c_void_p
+A16 = P(0x10000)          # fake, 16-byte aligned device addresses: never dereferenced,
+A16b = P(0x20000)         # the calls below all fail argument checks first
+A16c = P(0x30000)
+MIS = P(0x10004)
+
+
+def test_quant_argument_checks(lib):
+    f = lib.fp8q_quant_act_1x128
+    assert f(None, 1, 128, 128, A16b, A16c, None) == 1        # null input
+    assert f(A16, 7, 128, 128, A16b, A16c, None) == 1         # bad dtype
+    assert f(A16, 1, 0, 128, A16b, A16c, None) == 1           # empty
+    assert f(A16, 1, 128, 200, A16b, A16c, None) == 2         # ragged K
+    assert f(MIS, 1, 128, 128, A16b, A16c, None) == 3         # misaligned input
+    g = lib.fp8q_quant_act_128x1
+    assert g(A16, 1, 100, 64, A16b, A16c, None) == 2          # T not multiple of 128
+    assert g(A16, 1, 128, 96, A16b, A16c, None) == 2          # C not multiple of 64
+    h = lib.fp8q_quant_w_128x128
+    assert h(A16, 1, 130, 128, A16b, A16c, None) == 2
+    assert h(A16, 0, 128, 128, MIS, A16c, None) == 3
+
+
+def test_gemm_argument_checks(lib):
+    g = lib.fp8q_gemm_ex
+    ok = (A16, A16b, A16c, P(0x40000), P(0x50000))
+    assert g(None, *ok[1:], 128, 128, 128, 0, 0, None) == 1
+    assert g(*ok, 128, 128, 128, 3, 0, None) == 1               # bad out dtype
+    assert g(*ok, 128, 128, 128, 0, 9, None) == 1               # bad scale mode
+    assert g(*ok, 100, 128, 128, 0, 0, None) == 2               # ragged M
+    assert g(*ok, 128, 136, 128, 0, 0, None) == 2               # ragged N
+    assert g(*ok, 128, 128, 64, 0, 0, None) == 2                # ragged K
+    assert g(*ok, -128, 128, 128, 0, 0, None) == 1
+    assert g(MIS, *ok[1:], 128, 128, 128, 0, 0, None) == 3
+    gg = lib.fp8q_gemm_grouped
+    assert gg(*ok, None, 4, 512, 128, 128, 1, None) == 1       # no offsets
+    assert gg(*ok, A16, 0, 512, 128, 128, 1, None) == 2        # no groups
+    assert gg(*ok, A16, 513, 512, 128, 128, 1, None) == 2      # too many groups
+    assert gg(*ok, P(0x10002), 4, 512, 128, 128, 1, None) == 3  # misaligned offsets
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    import torch
+
+    import fp8_fine_grained_21_b300 as fq
+
+    x = torch.zeros(128, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        fq.quant_act_1x128(x)
