@@ -17,10 +17,11 @@
 //     128-K block into one of two TMEM buffers (128 lanes x BN FP32
 //     columns), a fresh accumulation per block; tcgen05.commit releases the
 //     smem stage and signals the promotion warps;
-//   * BN/128 promotion warpgroups: tcgen05.ld the partial (warp w reads TMEM
-//     lanes 32 (w%4) .. +31, warpgroup j columns 128 j .. +127), release the
-//     TMEM buffer, and accumulate P * (sA * sB) into 128 FP32 registers per
-//     thread with packed FP32 FMAs; after the last block, write C.
+//   * 4*BN/128 promotion warps: tcgen05.ld the partial in 16-column chunks
+//     (the next chunk's load in flight while the current one is scaled),
+//     release the TMEM buffer once the last chunk has arrived, and accumulate
+//     P * (sA * sB) into 128 FP32 registers per thread with packed FP32
+//     FMAs; after the last block, write C.
 // The MMA of block i+1 (other TMEM buffer) overlaps the promotion of block i.
 // Persistent: one CTA per SM walks tiles blockIdx.x, +gridDim.x, ...; the
 // rings carry over from one tile to the next.
@@ -38,23 +39,20 @@ constexpr int kBK = 128;          // K per block = scale-group width = one 128-b
 constexpr int kScaleSlots = 8;
 constexpr int kMaxGroups = 512;
 
-// Warp roles: warpgroup 0 = {producer, MMA, idle, idle}; warpgroups 1..kWG
-// promote.  Warps are spread over the four SM sub-partitions by warp index,
-// so each sub-partition holds one control warp and kWG promotion warps.
+// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
+// warps 2 .. 2 + 4*BN/128 - 1 promote.  A warp may only read the TMEM lanes
+// 32*(warp % 4) .. +31, so promotion warp w takes lane quarter w % 4 and the
+// 128-column half (w - 2) / 4 of the tile: each thread owns one row of the
+// tile and 128 FP32 accumulators.  No register reallocation is needed: with
+// 320 threads (BN = 256) every thread may hold 200 registers.
 template <int BN>
 struct GemmShape {
-    static constexpr int kWG = BN / 128;                 // promotion warpgroups
-    static constexpr int kPromoWarps = 4 * kWG;
+    static constexpr int kHalves = BN / 128;             // 128-column halves of the tile
+    static constexpr int kPromoWarps = 4 * kHalves;
     static constexpr int kProducerWarp = 0;
     static constexpr int kMmaWarp = 1;
-    static constexpr int kFirstPromoWarp = 4;
-    static constexpr int kThreads = 128 * (kWG + 1);
-    // Register split for BN = 256 (384 threads launch with 168 each = 64512):
-    // control warpgroup 40, promotion warpgroups 232: 128*40 + 256*232 = 64512.
-    static constexpr int kCtrlRegs = 40;
-    static constexpr int kPromoRegs = 232;
-    static_assert(kWG == 1 || 128 * kCtrlRegs + 128 * kWG * kPromoRegs <= kThreads * 168,
-                  "register split exceeds the launch allocation");
+    static constexpr int kFirstPromoWarp = 2;
+    static constexpr int kThreads = 32 * (kFirstPromoWarp + kPromoWarps);
     static constexpr int kStages = BN == 256 ? 4 : 6;
     static constexpr int kABytes = kBM * kBK;
     static constexpr int kBBytes = BN * kBK;
@@ -85,6 +83,36 @@ struct GemmArgs {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// acc[j] += (P[2j], P[2j+1]) * scale for the W columns of one TMEM chunk.
+// Block-scaled B: one factor f = sA * sB for the whole row segment.
+// Row-scaled B (weight gradient): factor fa * sB[n] per column n.
+template <bool kRowB, int W>
+__device__ __forceinline__ void promote_chunk(float2* acc, const uint32_t (&r)[W], float f,
+                                              float fa, const float* sb) {
+    if (!kRowB) {
+        const float2 ff = make_float2(f, f);
+#pragma unroll
+        for (int j = 0; j < W / 2; ++j)
+            acc[j] = __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])),
+                                ff, acc[j]);
+    } else {
+        const float2 fa2 = make_float2(fa, fa);
+        const float4* sb4 = reinterpret_cast<const float4*>(sb);
+#pragma unroll
+        for (int j4 = 0; j4 < W / 4; ++j4) {
+            const float4 q = sb4[j4];
+            const float2 f01 = __fmul2_rn(fa2, make_float2(q.x, q.y));
+            const float2 f23 = __fmul2_rn(fa2, make_float2(q.z, q.w));
+            acc[2 * j4] = __ffma2_rn(
+                make_float2(__uint_as_float(r[4 * j4]), __uint_as_float(r[4 * j4 + 1])), f01,
+                acc[2 * j4]);
+            acc[2 * j4 + 1] = __ffma2_rn(
+                make_float2(__uint_as_float(r[4 * j4 + 2]), __uint_as_float(r[4 * j4 + 3])), f23,
+                acc[2 * j4 + 1]);
+        }
+    }
 }
 
 // Tile t -> A row of the tile, B row (in the [G*N] view), first column, group.
@@ -195,7 +223,6 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
     const int num_tiles = static_cast<int>(misc[1]);
 
     if (warp < S::kFirstPromoWarp) {
-        if (S::kWG > 1) setmaxnreg_dec<S::kCtrlRegs>();
         if (warp == S::kProducerWarp && lane == 0) {
             // -------------------------------------------------- producer
             uint32_t stage = 0, phase = 0, slot = 0, sphase = 0;
@@ -268,20 +295,19 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
         }
     } else {
         // ----------------------------------------------------- promotion
-        if (S::kWG > 1) setmaxnreg_inc<S::kPromoRegs>();
-        const int wg = (warp >> 2) - 1, quarter = warp & 3;
+        const int half = (warp - S::kFirstPromoWarp) >> 2, quarter = warp & 3;
         const int row = quarter * 32 + lane;       // TMEM lane = row of the tile
         uint32_t it = 0, slot = 0, sphase = 0;
         bool ok = true;
-        float acc[128];
+        float2 acc[64];                            // columns 2j, 2j+1 of this thread's half
 #pragma unroll 1
         for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
             const TileCoord tc = decode_tile<BN>(t, grouped, N, args.G, gtile, grow);
             const float* sb_blk = nullptr;
             if (!kRowB)
-                sb_blk = args.sB + (static_cast<size_t>(tc.e) * (N / 128) + (tc.n0 / 128 + wg)) * Kb;
+                sb_blk = args.sB + (static_cast<size_t>(tc.e) * (N / 128) + (tc.n0 / 128 + half)) * Kb;
 #pragma unroll
-            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+            for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
 #pragma unroll 1
             for (int kb = 0; kb < Kb; ++kb, ++it) {
                 const uint32_t b = it & 1, tph = (it >> 1) & 1;
@@ -293,53 +319,37 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
                 const float* sl =
                     reinterpret_cast<const float*>(smem + S::kOffScale + slot * S::kSlotBytes);
                 const float fa = sl[row];
+                const float* sbc = sl + kBM + half * 128;   // row-mode B scales of this half
                 if (!__all_sync(0xffffffffu, mbar_wait(&tfull[b], tph, args.status))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t taddr =
-                    tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * BN + wg * 128;
+                    tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * BN + half * 128;
                 const float f = fa * fb;
+                // Chunks of kCW columns; the load of chunk c+1 is in flight while
+                // chunk c is scaled and added.  The TMEM buffer is handed back to
+                // the MMA warp as soon as the last chunk has arrived.
+                constexpr int kCW = kRowB ? 8 : 16;
+                constexpr int kNC = 128 / kCW;
+                uint32_t r0[kCW], r1[kCW];
+                tmem_ld_chunk(taddr, r0);
+                tmem_ld_wait(r0);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(taddr + c * 32, r);
-                    tmem_ld_wait(r);
-                    if (c == 3) {
+                for (int c = 0; c < kNC; c += 2) {
+                    tmem_ld_chunk(taddr + (c + 1) * kCW, r1);
+                    promote_chunk<kRowB>(acc + c * (kCW / 2), r0, f, fa, sbc + c * kCW);
+                    tmem_ld_wait(r1);
+                    if (c + 2 < kNC) {
+                        tmem_ld_chunk(taddr + (c + 2) * kCW, r0);
+                    } else {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&tempty[b]);
                     }
-                    if (!kRowB) {
-                        const float2 ff = make_float2(f, f);
-#pragma unroll
-                        for (int j = 0; j < 32; j += 2) {
-                            float2 a2 = make_float2(acc[c * 32 + j], acc[c * 32 + j + 1]);
-                            a2 = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                                            ff, a2);
-                            acc[c * 32 + j] = a2.x;
-                            acc[c * 32 + j + 1] = a2.y;
-                        }
-                    } else {
-                        const float4* sbv = reinterpret_cast<const float4*>(sl + kBM + wg * 128 + c * 32);
-                        const float2 fa2 = make_float2(fa, fa);
-#pragma unroll
-                        for (int j4 = 0; j4 < 8; ++j4) {
-                            const float4 q = sbv[j4];
-                            const float2 f01 = __fmul2_rn(fa2, make_float2(q.x, q.y));
-                            const float2 f23 = __fmul2_rn(fa2, make_float2(q.z, q.w));
-                            const int j = c * 32 + 4 * j4;
-                            float2 a01 = make_float2(acc[j], acc[j + 1]);
-                            float2 a23 = make_float2(acc[j + 2], acc[j + 3]);
-                            a01 = __ffma2_rn(make_float2(__uint_as_float(r[4 * j4]),
-                                                         __uint_as_float(r[4 * j4 + 1])), f01, a01);
-                            a23 = __ffma2_rn(make_float2(__uint_as_float(r[4 * j4 + 2]),
-                                                         __uint_as_float(r[4 * j4 + 3])), f23, a23);
-                            acc[j] = a01.x; acc[j + 1] = a01.y;
-                            acc[j + 2] = a23.x; acc[j + 3] = a23.y;
-                        }
-                    }
+                    promote_chunk<kRowB>(acc + (c + 1) * (kCW / 2), r1, f, fa, sbc + (c + 1) * kCW);
+                    if (c + 2 < kNC) tmem_ld_wait(r0);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sempty[slot]);
@@ -348,24 +358,24 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
             if (!ok) break;
             // ------------------------------------------------ epilogue
             const size_t crow = static_cast<size_t>(tc.arow + row);
-            const int ccol = tc.n0 + wg * 128;
+            const int ccol = tc.n0 + half * 128;
             if (kBf16Out) {
                 __nv_bfloat16* cp = reinterpret_cast<__nv_bfloat16*>(args.C) + crow * N + ccol;
 #pragma unroll
-                for (int j = 0; j < 128; j += 8) {
+                for (int j = 0; j < 64; j += 4) {
                     uint4 v;
-                    v.x = pack_bf16x2(acc[j], acc[j + 1]);
-                    v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
-                    v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
-                    v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
-                    *reinterpret_cast<uint4*>(cp + j) = v;
+                    v.x = pack_bf16x2(acc[j].x, acc[j].y);
+                    v.y = pack_bf16x2(acc[j + 1].x, acc[j + 1].y);
+                    v.z = pack_bf16x2(acc[j + 2].x, acc[j + 2].y);
+                    v.w = pack_bf16x2(acc[j + 3].x, acc[j + 3].y);
+                    *reinterpret_cast<uint4*>(cp + 2 * j) = v;
                 }
             } else {
                 float* cp = reinterpret_cast<float*>(args.C) + crow * N + ccol;
 #pragma unroll
-                for (int j = 0; j < 128; j += 4)
-                    *reinterpret_cast<float4*>(cp + j) =
-                        make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                for (int j = 0; j < 64; j += 2)
+                    *reinterpret_cast<float4*>(cp + 2 * j) =
+                        make_float4(acc[j].x, acc[j].y, acc[j + 1].x, acc[j + 1].y);
             }
         }
         tc_fence_before();

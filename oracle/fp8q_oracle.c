@@ -21,7 +21,7 @@
  * The E4M3 bit layout itself is not printed on the pages; it is the OCP 8-bit
  * floating-point definition (bias 7, no infinities, S.1111.111 = NaN).
  *
- * Readings taken where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - max representable E4M3 value = 448; cast = round-to-nearest-even with
  *     saturation to +-448; NaN -> 0x7F; the sign of zero is kept.
  *   - tile scale s = fl32(amax / 448); elements are multiplied by
