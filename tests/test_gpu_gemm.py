@@ -200,23 +200,57 @@ def test_grouped_bad_offsets_reported(fq, oracle, bad):
 
 
 # ------------------------------------------------------------ full workloads
-def _device_quant_forward(fq, d):
-    a8, sa = fq.quant_act_1x128(to_dev(d["A"]))
-    w8, sw = fq.quant_w_128x128(to_dev(d["W"]))
-    return a8, sa, w8, sw
+# The oracle quantizes only what the sampled outputs depend on: 1x128 tiles
+# and 128x1 tiles belong to one row (channel), so a row subset is exact; a
+# 128x128 block needs its whole 128 rows of W.  Every 128 x 128 output tile
+# contributes its four corners; random entries come on top.
+def corner_and_random(n, k, rng):
+    corners = np.concatenate([np.arange(0, n, 128), np.arange(127, n, 128)])
+    return np.unique(np.concatenate([corners, rng.integers(0, n, k)])).astype(np.int64)
+
+
+def compact_entries(rows, cols, rng, extra=4096):
+    """All (row, col) pairs where both are tile corners, plus random pairs,
+    as indices into the compact row / column lists."""
+    rc = np.flatnonzero((rows % 128 == 0) | (rows % 128 == 127))
+    cc = np.flatnonzero((cols % 128 == 0) | (cols % 128 == 127))
+    mi = np.repeat(rc, len(cc))
+    ni = np.tile(cc, len(rc))
+    mi = np.concatenate([mi, rng.integers(0, len(rows), extra)])
+    ni = np.concatenate([ni, rng.integers(0, len(cols), extra)])
+    return mi.astype(np.int64), ni.astype(np.int64)
+
+
+def check_sampled(Cg, rows, cols, A8c, sAc, B8c, sBc, bmode, bf16, what, rng):
+    """Cg: the GPU result on the host.  A8c/sAc: operand A restricted to `rows`;
+    B8c/sBc: operand B restricted to `cols` (compact index spaces)."""
+    mi, ni = compact_entries(rows, cols, rng)
+    Cref, Cabs = oracle_mod().gemm_entries(A8c, sAc, B8c, sBc, mi, ni, bmode=bmode)
+    got = Cg[rows[mi], cols[ni]]
+    assert_gemm_close(got, Cref, Cabs, bf16, what)
+
+
+def oracle_mod():
+    import oracle
+    return oracle
 
 
 @pytest.mark.slow
 def test_forward_workload_sampled(fq, oracle):
     d = fi.make("forward")
-    a8, sa, w8, sw = _device_quant_forward(fq, d)
+    a8, sa = fq.quant_act_1x128(to_dev(d["A"]))
+    w8, sw = fq.quant_w_128x128(to_dev(d["W"]))
     C = fq.gemm(a8, sa, w8, sw, out_dtype=torch.bfloat16)
     assert fq.fp8q_get_device_status() == 0
-    A8o, sAo = oracle.quant_1x128(d["A"])
+    rng = np.random.default_rng(11)
+    rows = corner_and_random(4096, 32, rng)
+    cols = corner_and_random(2048, 32, rng)
+    A8o, sAo = oracle.quant_1x128(d["A"][rows])
     B8o, sBo = oracle.quant_128x128(d["W"])
-    mi, ni = sample_entries(4096, 2048, 256, np.random.default_rng(11), extra=1024)
-    Cref, Cabs = oracle.gemm_entries(A8o, sAo, B8o, sBo, mi, ni)
-    assert_gemm_close(cpu(C)[mi, ni], Cref, Cabs, True, "forward workload")
+    # columns of the compact B: 1x128-style per-column scales expanded from the blocks
+    B8c = np.ascontiguousarray(B8o[cols])
+    sBc = np.ascontiguousarray(sBo[cols // 128].T)           # [Kb][n_cols]
+    check_sampled(cpu(C), rows, cols, A8o, sAo, B8c, sBc, 1, True, "forward workload", rng)
 
 
 @pytest.mark.slow
@@ -226,11 +260,15 @@ def test_accum_workload_sampled(fq, oracle, variant):
     a8, sa = fq.quant_act_1x128(to_dev(d["A"]))
     b8, sb = fq.quant_w_128x128(to_dev(d["B"]))
     C = fq.gemm(a8, sa, b8, sb, out_dtype=torch.float32)
-    A8o, sAo = oracle.quant_1x128(d["A"])
+    assert fq.fp8q_get_device_status() == 0
+    rng = np.random.default_rng(12)
+    rows = corner_and_random(1024, 32, rng)
+    cols = corner_and_random(1024, 32, rng)
+    A8o, sAo = oracle.quant_1x128(d["A"][rows])
     B8o, sBo = oracle.quant_128x128(d["B"])
-    mi, ni = sample_entries(1024, 1024, 256, np.random.default_rng(12), extra=1024)
-    Cref, Cabs = oracle.gemm_entries(A8o, sAo, B8o, sBo, mi, ni)
-    assert_gemm_close(cpu(C)[mi, ni], Cref, Cabs, False, "accum workload " + variant)
+    B8c = np.ascontiguousarray(B8o[cols])
+    sBc = np.ascontiguousarray(sBo[cols // 128].T)
+    check_sampled(cpu(C), rows, cols, A8o, sAo, B8c, sBc, 1, False, "accum workload " + variant, rng)
 
 
 @pytest.mark.slow
@@ -240,11 +278,12 @@ def test_wgrad_workload_sampled(fq, oracle):
     b8, sb = fq.quant_act_128x1(to_dev(d["X"]))
     C = fq.gemm(a8, sa, b8, sb, out_dtype=torch.float32, bscale=fq.BSCALE_ROW1x128)
     assert fq.fp8q_get_device_status() == 0
-    A8o, sAo = oracle.quant_128x1(d["dY"])
-    B8o, sBo = oracle.quant_128x1(d["X"])
-    mi, ni = sample_entries(7168, 2048, 256, np.random.default_rng(13), extra=512)
-    Cref, Cabs = oracle.gemm_entries(A8o, sAo, B8o, sBo, mi, ni, bmode=1)
-    assert_gemm_close(cpu(C)[mi, ni], Cref, Cabs, False, "wgrad workload")
+    rng = np.random.default_rng(13)
+    rows = corner_and_random(7168, 32, rng)                  # channels of dY
+    cols = corner_and_random(2048, 32, rng)                  # channels of X
+    A8o, sAo = oracle.quant_128x1(np.ascontiguousarray(d["dY"][:, rows]))
+    B8o, sBo = oracle.quant_128x1(np.ascontiguousarray(d["X"][:, cols]))
+    check_sampled(cpu(C), rows, cols, A8o, sAo, B8o, sBo, 1, False, "wgrad workload", rng)
 
 
 @pytest.mark.slow
@@ -259,18 +298,21 @@ def test_grouped_workload_sampled(fq, oracle):
                          to_dev(offs.astype(np.int32)))
     assert fq.fp8q_get_device_status() == 0
     rng = np.random.default_rng(14)
-    A8o, sAo = oracle.quant_1x128(A)
-    # oracle-quantized weights of a few experts only (each expert is independent)
-    experts = sorted(set([0, G - 1] + list(rng.integers(0, G, 4))))
-    mi, ni = [], []
-    B8o = np.zeros((G, N, K), np.uint8)
-    sBo = np.ones((G, N // 128, K // 128), np.float32)
+    Cg = cpu(C)
+    experts = sorted(set([0, G - 1] + [int(e) for e in rng.integers(0, G, 4)]))
+    checked = 0
     for e in experts:
-        B8o[e], sBo[e] = oracle.quant_128x128(W[e])
-        r0, r1 = offs[e], offs[e + 1]
-        if r1 > r0:
-            mi += list(rng.integers(r0, r1, 128)) + [r0, r1 - 1]
-            ni += list(rng.integers(0, N, 128)) + [0, N - 1]
-    mi, ni = np.array(mi, np.int64), np.array(ni, np.int64)
-    Cref, Cabs = oracle.gemm_grouped_entries(A8o, sAo, B8o, sBo, offs, mi, ni)
-    assert_gemm_close(cpu(C)[mi, ni], Cref, Cabs, True, "grouped workload")
+        r0, r1 = int(offs[e]), int(offs[e + 1])
+        if r1 == r0:
+            continue
+        # first and last row of every 128-row tile of the group, plus random rows
+        rows = np.unique(np.concatenate([np.arange(r0, r1, 128), np.arange(r0 + 127, r1, 128),
+                                         rng.integers(r0, r1, 8)])).astype(np.int64)
+        nbs = sorted(set([0, N // 128 - 1, int(rng.integers(0, N // 128))]))
+        cols = np.concatenate([np.arange(nb * 128, nb * 128 + 128) for nb in nbs]).astype(np.int64)
+        A8o, sAo = oracle.quant_1x128(A[rows])
+        B8o = np.concatenate([oracle.quant_128x128(W[e, nb * 128:nb * 128 + 128])[0] for nb in nbs])
+        sBo = np.concatenate([oracle.quant_128x128(W[e, nb * 128:nb * 128 + 128])[1] for nb in nbs])
+        check_sampled(Cg, rows, cols, A8o, sAo, B8o, sBo, 0, True, "grouped expert %d" % e, rng)
+        checked += 1
+    assert checked >= 2
