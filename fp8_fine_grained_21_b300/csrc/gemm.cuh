@@ -17,11 +17,11 @@
 //     128-K block into one of two TMEM buffers (128 lanes x BN FP32
 //     columns), a fresh accumulation per block; tcgen05.commit releases the
 //     smem stage and signals the promotion warps;
-//   * 4*BN/128 promotion warps: tcgen05.ld the partial in 16-column chunks
-//     (the next chunk's load in flight while the current one is scaled),
-//     release the TMEM buffer once the last chunk has arrived, and accumulate
-//     P * (sA * sB) into 128 FP32 registers per thread with packed FP32
-//     FMAs; after the last block, write C.
+//   * BN/128 promotion warpgroups: tcgen05.ld the partial in 16-column
+//     chunks (8 for row-scaled B), the next chunk's load in flight while the
+//     current one is scaled, release the TMEM buffer once the last chunk has
+//     arrived, and accumulate P * (sA * sB) into 128 FP32 registers per thread
+//     with packed FP32 FMAs; after the last block, write C.
 // The MMA of block i+1 (other TMEM buffer) overlaps the promotion of block i.
 // Persistent: one CTA per SM walks tiles blockIdx.x, +gridDim.x, ...; the
 // rings carry over from one tile to the next.
@@ -39,20 +39,31 @@ constexpr int kBK = 128;          // K per block = scale-group width = one 128-b
 constexpr int kScaleSlots = 8;
 constexpr int kMaxGroups = 512;
 
-// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
-// warps 2 .. 2 + 4*BN/128 - 1 promote.  A warp may only read the TMEM lanes
-// 32*(warp % 4) .. +31, so promotion warp w takes lane quarter w % 4 and the
-// 128-column half (w - 2) / 4 of the tile: each thread owns one row of the
-// tile and 128 FP32 accumulators.  No register reallocation is needed: with
-// 320 threads (BN = 256) every thread may hold 200 registers.
+// Warp roles, by warpgroup (four consecutive warps, one on each SM
+// sub-partition): warpgroup 0 = control (warp 0 = TMA producer, warp kMmaWarp
+// = MMA issuer and TMEM owner, the other two idle); warpgroup 1 + h promotes
+// the 128-column half h of the tile.  A warp may only read the TMEM lanes
+// 32*(warp % 4) .. +31, so promotion warp w takes lane quarter w % 4: each
+// thread owns one row of the tile and 128 FP32 accumulators.  For BN = 256
+// the control warpgroup gives registers up to the promotion warpgroups
+// (setmaxnreg): per sub-partition 56 + 2 * 224 = 504 <= 512 registers a lane.
+#ifndef FP8Q_MMA_WARP
+#define FP8Q_MMA_WARP 1
+#endif
 template <int BN>
 struct GemmShape {
     static constexpr int kHalves = BN / 128;             // 128-column halves of the tile
     static constexpr int kPromoWarps = 4 * kHalves;
     static constexpr int kProducerWarp = 0;
-    static constexpr int kMmaWarp = 1;
-    static constexpr int kFirstPromoWarp = 2;
-    static constexpr int kThreads = 32 * (kFirstPromoWarp + kPromoWarps);
+    static constexpr int kMmaWarp = FP8Q_MMA_WARP;
+    static constexpr int kFirstPromoWarp = 4;
+    static constexpr int kThreads = 128 * (1 + kHalves);
+    static constexpr bool kRealloc = kHalves > 1;
+    static constexpr int kCtrlRegs = 56;
+    static constexpr int kPromoRegs = 224;
+    static_assert(!kRealloc || 128 * kCtrlRegs + 128 * kHalves * kPromoRegs <= kThreads * 168,
+                  "register split exceeds the launch allocation");
+    static_assert(kMmaWarp > 0 && kMmaWarp < 4, "MMA warp must be a control warp");
     static constexpr int kStages = BN == 256 ? 4 : 6;
     static constexpr int kABytes = kBM * kBK;
     static constexpr int kBBytes = BN * kBK;
@@ -223,6 +234,7 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
     const int num_tiles = static_cast<int>(misc[1]);
 
     if (warp < S::kFirstPromoWarp) {
+        if (S::kRealloc) setmaxnreg_dec<S::kCtrlRegs>();
         if (warp == S::kProducerWarp && lane == 0) {
             // -------------------------------------------------- producer
             uint32_t stage = 0, phase = 0, slot = 0, sphase = 0;
@@ -239,15 +251,18 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
                     tma_load_2d(sa + S::kABytes, &tmB, &full[stage], kb * kBK, tc.brow);
                     if (++stage == S::kStages) { stage = 0; phase ^= 1; }
 
-                    if (!mbar_wait(&sempty[slot], sphase ^ 1, args.status)) { ok = false; break; }
-                    float* sl = reinterpret_cast<float*>(smem + S::kOffScale + slot * S::kSlotBytes);
-                    mbar_arrive_expect_tx(&sfull[slot], kRowB ? S::kSlotBytes : S::kSaBytes);
-                    bulk_load(sl, args.sA + static_cast<size_t>(kb) * args.M_total + tc.arow,
-                              S::kSaBytes, &sfull[slot]);
-                    if (kRowB)
+                    if (kRowB) {
+                        // weight-gradient form: both operands' 1x128 scales of
+                        // this block go through a shared-memory slot
+                        if (!mbar_wait(&sempty[slot], sphase ^ 1, args.status)) { ok = false; break; }
+                        float* sl = reinterpret_cast<float*>(smem + S::kOffScale + slot * S::kSlotBytes);
+                        mbar_arrive_expect_tx(&sfull[slot], S::kSlotBytes);
+                        bulk_load(sl, args.sA + static_cast<size_t>(kb) * args.M_total + tc.arow,
+                                  S::kSaBytes, &sfull[slot]);
                         bulk_load(sl + kBM, args.sB + static_cast<size_t>(kb) * N + tc.n0,
                                   S::kSbBytes, &sfull[slot]);
-                    if (++slot == kScaleSlots) { slot = 0; sphase ^= 1; }
+                        if (++slot == kScaleSlots) { slot = 0; sphase ^= 1; }
+                    }
                 }
             }
         } else if (warp == S::kMmaWarp && lane == 0) {
@@ -295,6 +310,7 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
         }
     } else {
         // ----------------------------------------------------- promotion
+        if (S::kRealloc) setmaxnreg_inc<S::kPromoRegs>();
         const int half = (warp - S::kFirstPromoWarp) >> 2, quarter = warp & 3;
         const int row = quarter * 32 + lane;       // TMEM lane = row of the tile
         uint32_t it = 0, slot = 0, sphase = 0;
@@ -303,23 +319,41 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
 #pragma unroll 1
         for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
             const TileCoord tc = decode_tile<BN>(t, grouped, N, args.G, gtile, grow);
-            const float* sb_blk = nullptr;
-            if (!kRowB)
-                sb_blk = args.sB + (static_cast<size_t>(tc.e) * (N / 128) + (tc.n0 / 128 + half)) * Kb;
+            // Block-scaled B: this thread's row scale and the 128x128 block scale
+            // are read straight from global memory (coalesced), one block ahead.
+            const float* sa_row = args.sA + tc.arow + row;
+            const float* sb_blk =
+                args.sB + (static_cast<size_t>(tc.e) * (N / 128) + (tc.n0 / 128 + half)) * Kb;
+            float fa_next = 0.0f, fb_next = 0.0f;
+            if (!kRowB) {
+                fa_next = __ldg(sa_row);
+                fb_next = __ldg(sb_blk);
+            }
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
 #pragma unroll 1
             for (int kb = 0; kb < Kb; ++kb, ++it) {
                 const uint32_t b = it & 1, tph = (it >> 1) & 1;
-                const float fb = kRowB ? 1.0f : __ldg(sb_blk + kb);
-                if (!__all_sync(0xffffffffu, mbar_wait(&sfull[slot], sphase, args.status))) {
-                    ok = false;
-                    break;
+                float fa, f;
+                const float* sbc = nullptr;
+                if (!kRowB) {
+                    fa = fa_next;
+                    f = fa_next * fb_next;
+                    if (kb + 1 < Kb) {
+                        fa_next = __ldg(sa_row + static_cast<size_t>(kb + 1) * args.M_total);
+                        fb_next = __ldg(sb_blk + kb + 1);
+                    }
+                } else {
+                    if (!__all_sync(0xffffffffu, mbar_wait(&sfull[slot], sphase, args.status))) {
+                        ok = false;
+                        break;
+                    }
+                    const float* sl =
+                        reinterpret_cast<const float*>(smem + S::kOffScale + slot * S::kSlotBytes);
+                    fa = sl[row];
+                    f = fa;
+                    sbc = sl + kBM + half * 128;     // this half's 1x128 B scales
                 }
-                const float* sl =
-                    reinterpret_cast<const float*>(smem + S::kOffScale + slot * S::kSlotBytes);
-                const float fa = sl[row];
-                const float* sbc = sl + kBM + half * 128;   // row-mode B scales of this half
                 if (!__all_sync(0xffffffffu, mbar_wait(&tfull[b], tph, args.status))) {
                     ok = false;
                     break;
@@ -327,33 +361,53 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
                 tc_fence_after();
                 const uint32_t taddr =
                     tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * BN + half * 128;
-                const float f = fa * fb;
-                // Chunks of kCW columns; the load of chunk c+1 is in flight while
-                // chunk c is scaled and added.  The TMEM buffer is handed back to
-                // the MMA warp as soon as the last chunk has arrived.
-                constexpr int kCW = kRowB ? 8 : 16;
-                constexpr int kNC = 128 / kCW;
-                uint32_t r0[kCW], r1[kCW];
-                tmem_ld_chunk(taddr, r0);
-                tmem_ld_wait(r0);
+                if (!kRowB) {
+                    // Sixteen-column chunks, the next chunk's load in flight while
+                    // the current one is scaled; the TMEM buffer goes back to the
+                    // MMA warp as soon as the last chunk has arrived.
+                    uint32_t r0[16], r1[16];
+                    tmem_ld_chunk(taddr, r0);
+                    tmem_ld_wait(r0);
 #pragma unroll
-                for (int c = 0; c < kNC; c += 2) {
-                    tmem_ld_chunk(taddr + (c + 1) * kCW, r1);
-                    promote_chunk<kRowB>(acc + c * (kCW / 2), r0, f, fa, sbc + c * kCW);
-                    tmem_ld_wait(r1);
-                    if (c + 2 < kNC) {
-                        tmem_ld_chunk(taddr + (c + 2) * kCW, r0);
-                    } else {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&tempty[b]);
+                    for (int c = 0; c < 8; c += 2) {
+                        tmem_ld_chunk(taddr + (c + 1) * 16, r1);
+                        promote_chunk<false>(acc + c * 8, r0, f, fa, nullptr);
+                        tmem_ld_wait(r1);
+                        if (c + 2 < 8) {
+                            tmem_ld_chunk(taddr + (c + 2) * 16, r0);
+                        } else {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&tempty[b]);
+                        }
+                        promote_chunk<false>(acc + (c + 1) * 8, r1, f, fa, nullptr);
+                        if (c + 2 < 8) tmem_ld_wait(r0);
                     }
-                    promote_chunk<kRowB>(acc + (c + 1) * (kCW / 2), r1, f, fa, sbc + (c + 1) * kCW);
-                    if (c + 2 < kNC) tmem_ld_wait(r0);
+                } else {
+                    // Eight-column chunks, the next chunk's load in flight while
+                    // the current one is scaled.
+                    uint32_t r0[8], r1[8];
+                    tmem_ld_chunk(taddr, r0);
+                    tmem_ld_wait(r0);
+#pragma unroll
+                    for (int c = 0; c < 16; c += 2) {
+                        tmem_ld_chunk(taddr + (c + 1) * 8, r1);
+                        promote_chunk<true>(acc + c * 4, r0, f, fa, sbc + c * 8);
+                        tmem_ld_wait(r1);
+                        if (c + 2 < 16) {
+                            tmem_ld_chunk(taddr + (c + 2) * 8, r0);
+                        } else {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&tempty[b]);
+                        }
+                        promote_chunk<true>(acc + (c + 1) * 4, r1, f, fa, sbc + (c + 1) * 8);
+                        if (c + 2 < 16) tmem_ld_wait(r0);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sempty[slot]);
+                    if (++slot == kScaleSlots) { slot = 0; sphase ^= 1; }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sempty[slot]);
-                if (++slot == kScaleSlots) { slot = 0; sphase ^= 1; }
             }
             if (!ok) break;
             // ------------------------------------------------ epilogue
