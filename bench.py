@@ -183,6 +183,8 @@ class Workload:
             self.a8, self.sa = fq.quant_act_1x128(x0)
             self.b8, self.sb = fq.quant_w_128x128(x1)
         self.C = torch.empty((self.M, self.N), dtype=self.out_dtype, device=device)
+        # stream-K workspace (counters start at zero; every call leaves them zero)
+        self.ws = torch.zeros(fq.fp8q_gemm_workspace_size(), dtype=torch.uint8, device=device)
         self.flops = 2.0 * self.M * self.N * self.K
         e0, e1 = x0.numel(), x1.numel()
         # algorithmic bytes: BF16 in + FP8 out + FP32 scales
@@ -210,13 +212,15 @@ class Workload:
     def gemm(self, stream=None):
         fq = self.fq
         if self.name == "grouped":
-            fq.fp8q_gemm_grouped(self.a8, self.sa, self.b8.view(self.G, self.N, self.K),
-                                 self.sb.view(self.G, self.N // 128, self.K // 128), self.C,
-                                 self.offs, stream)
+            fq.fp8q_gemm_grouped_ws(self.a8, self.sa, self.b8.view(self.G, self.N, self.K),
+                                    self.sb.view(self.G, self.N // 128, self.K // 128), self.C,
+                                    self.offs, self.ws, stream)
         elif self.name == "wgrad":
-            fq.fp8q_gemm_ex(self.a8, self.sa, self.b8, self.sb, self.C, fq.BSCALE_ROW1x128, stream)
+            fq.fp8q_gemm_ws(self.a8, self.sa, self.b8, self.sb, self.C, fq.BSCALE_ROW1x128,
+                            self.ws, stream)
         else:
-            fq.fp8q_gemm_ex(self.a8, self.sa, self.b8, self.sb, self.C, fq.BSCALE_BLOCK128, stream)
+            fq.fp8q_gemm_ws(self.a8, self.sa, self.b8, self.sb, self.C, fq.BSCALE_BLOCK128,
+                            self.ws, stream)
 
     def step(self, stream=None):
         self.quant0(stream)

@@ -16,8 +16,9 @@ import torch
 __all__ = [
     "Fp8qError", "library_path", "load",
     "fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128",
-    "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_get_device_status",
-    "fp8q_status_string", "fp8q_version",
+    "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_gemm_ws", "fp8q_gemm_grouped_ws",
+    "fp8q_gemm_workspace_size", "fp8q_get_device_status", "fp8q_status_string", "fp8q_version",
+    "workspace",
     "quant_act_1x128", "quant_act_128x1", "quant_w_128x128", "gemm", "gemm_grouped",
     "F32", "BF16", "BSCALE_BLOCK128", "BSCALE_ROW1x128",
 ]
@@ -31,7 +32,8 @@ STATUS_NAMES = {0: "FP8Q_OK", 1: "FP8Q_ERR_INVALID_ARG", 2: "FP8Q_ERR_UNSUPPORTE
                 3: "FP8Q_ERR_MISALIGNED", 4: "FP8Q_ERR_CUDA", 5: "FP8Q_ERR_TIMEOUT",
                 6: "FP8Q_ERR_BAD_GROUPS"}
 EXPORTS = ("fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128", "fp8q_gemm",
-           "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_get_device_status", "fp8q_status_string",
+           "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_gemm_ws", "fp8q_gemm_grouped_ws",
+           "fp8q_gemm_workspace_size", "fp8q_get_device_status", "fp8q_status_string",
            "fp8q_version")
 
 
@@ -68,6 +70,13 @@ def load():
     lib.fp8q_gemm_ex.restype = I
     lib.fp8q_gemm_grouped.argtypes = [P, P, P, P, P, P, I, I64, I64, I64, I, P]
     lib.fp8q_gemm_grouped.restype = I
+    SZ = ctypes.c_size_t
+    lib.fp8q_gemm_ws.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P]
+    lib.fp8q_gemm_ws.restype = I
+    lib.fp8q_gemm_grouped_ws.argtypes = [P, P, P, P, P, P, I, I64, I64, I64, I, P, SZ, P]
+    lib.fp8q_gemm_grouped_ws.restype = I
+    lib.fp8q_gemm_workspace_size.argtypes = []
+    lib.fp8q_gemm_workspace_size.restype = SZ
     lib.fp8q_get_device_status.argtypes = [P]
     lib.fp8q_get_device_status.restype = I
     lib.fp8q_status_string.argtypes = [I]
@@ -170,6 +179,57 @@ def fp8q_gemm_grouped(A8, sA, B8, sB, C, m_offsets, stream=None):
         G, Mtot, N, K, _out_dtype(C.dtype), _stream(stream)))
 
 
+def _ws(ws):
+    if ws is None:
+        return ctypes.c_void_p(None), 0
+    return _dev(ws, "workspace", torch.uint8), ws.numel()
+
+
+def fp8q_gemm_ws(A8, sA, B8, sB, C, bscale=BSCALE_BLOCK128, ws=None, stream=None):
+    M, K = A8.shape
+    N = B8.shape[0]
+    wp, wn = _ws(ws)
+    _check("fp8q_gemm_ws", load().fp8q_gemm_ws(
+        _dev(A8, "A8", torch.uint8), _dev(sA, "sA", torch.float32), _dev(B8, "B8", torch.uint8),
+        _dev(sB, "sB", torch.float32), _dev(C, "C"), M, N, K, _out_dtype(C.dtype), int(bscale),
+        wp, wn, _stream(stream)))
+
+
+def fp8q_gemm_grouped_ws(A8, sA, B8, sB, C, m_offsets, ws=None, stream=None):
+    Mtot, K = A8.shape
+    G, N, _ = B8.shape
+    wp, wn = _ws(ws)
+    _check("fp8q_gemm_grouped_ws", load().fp8q_gemm_grouped_ws(
+        _dev(A8, "A8", torch.uint8), _dev(sA, "sA", torch.float32), _dev(B8, "B8", torch.uint8),
+        _dev(sB, "sB", torch.float32), _dev(C, "C"), _dev(m_offsets, "m_offsets", torch.int32),
+        G, Mtot, N, K, _out_dtype(C.dtype), wp, wn, _stream(stream)))
+
+
+def fp8q_gemm_workspace_size() -> int:
+    return int(load().fp8q_gemm_workspace_size())
+
+
+_WORKSPACES = {}
+
+
+def workspace(device=None, stream=None):
+    """Zero-initialised stream-K workspace for (device, stream), allocated with
+    torch on first use and kept; calls leave its counters zero again."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    key = (dev.index, int(stream.cuda_stream) if isinstance(stream, torch.cuda.Stream) else int(stream))
+    ws = _WORKSPACES.get(key)
+    if ws is None:
+        with torch.cuda.device(dev):
+            n = fp8q_gemm_workspace_size()
+            if n == 0:
+                raise Fp8qError("fp8q_gemm_workspace_size", 4)
+            ws = torch.zeros(n, dtype=torch.uint8, device=dev)
+        _WORKSPACES[key] = ws
+    return ws
+
+
 def fp8q_get_device_status(stream=None) -> int:
     return int(load().fp8q_get_device_status(_stream(stream)))
 
@@ -214,15 +274,20 @@ def quant_w_128x128(w, stream=None):
     return q, s
 
 
-def gemm(A8, sA, B8, sB, out_dtype=torch.bfloat16, bscale=BSCALE_BLOCK128, stream=None):
-    """C[M][N] = dequant(A8) @ dequant(B8)^T."""
+def gemm(A8, sA, B8, sB, out_dtype=torch.bfloat16, bscale=BSCALE_BLOCK128, stream=None,
+         stream_k=True):
+    """C[M][N] = dequant(A8) @ dequant(B8)^T (stream-K over all SMs unless
+    stream_k=False)."""
     C = torch.empty((A8.shape[0], B8.shape[0]), dtype=out_dtype, device=A8.device)
-    fp8q_gemm_ex(A8, sA, B8, sB, C, bscale, stream)
+    ws = workspace(A8.device, stream) if stream_k else None
+    fp8q_gemm_ws(A8, sA, B8, sB, C, bscale, ws, stream)
     return C
 
 
-def gemm_grouped(A8, sA, B8, sB, m_offsets, out_dtype=torch.bfloat16, stream=None):
+def gemm_grouped(A8, sA, B8, sB, m_offsets, out_dtype=torch.bfloat16, stream=None,
+                 stream_k=True):
     """Grouped GEMM; rows outside every group are left unwritten (uninitialized)."""
     C = torch.empty((A8.shape[0], B8.shape[1]), dtype=out_dtype, device=A8.device)
-    fp8q_gemm_grouped(A8, sA, B8, sB, C, m_offsets, stream)
+    ws = workspace(A8.device, stream) if stream_k else None
+    fp8q_gemm_grouped_ws(A8, sA, B8, sB, C, m_offsets, ws, stream)
     return C

@@ -110,9 +110,19 @@ int launch_gemm_bn(DeviceState* d, const CUtensorMap& ta, const CUtensorMap& tb,
                 : launch_gemm_inst<BN, false, false>(d, ta, tb, args, tiles_upper, st);
 }
 
+// Stream-K workspace: arrival counters (one per promotion warp of each
+// stream-K tile; at most 2 * SMs such tiles), then FP32 partial tiles (at most
+// two per CTA, one CTA per SM), each a 128 x 256 float block.
+constexpr size_t kWsCounterBytes(int sms) {
+    return ((static_cast<size_t>(2) * sms * GemmShape<256>::kPromoWarps * sizeof(int) + 255) / 256) * 256;
+}
+constexpr size_t kWsPartialBytes(int sms) {
+    return static_cast<size_t>(2) * sms * (kBM * 256) * sizeof(float);
+}
+
 int gemm_common(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB, void* C,
                 const int* m_offsets, int G, int64_t M, int64_t N, int64_t K, int out_dtype,
-                int bscale, cudaStream_t st) {
+                int bscale, void* workspace, size_t ws_bytes, cudaStream_t st) {
     if (!A8 || !sA || !B8 || !sB || !C) return FP8Q_ERR_INVALID_ARG;
     if (out_dtype != FP8Q_F32 && out_dtype != FP8Q_BF16) return FP8Q_ERR_INVALID_ARG;
     if (bscale != FP8Q_BSCALE_BLOCK128 && bscale != FP8Q_BSCALE_ROW1x128) return FP8Q_ERR_INVALID_ARG;
@@ -127,6 +137,11 @@ int gemm_common(const uint8_t* A8, const float* sA, const uint8_t* B8, const flo
     DeviceState* d = nullptr;
     int rc = device_state(&d);
     if (rc != FP8Q_OK) return rc;
+    if (workspace) {
+        if (!aligned(workspace, 256)) return FP8Q_ERR_MISALIGNED;
+        if (ws_bytes < kWsCounterBytes(d->num_sms) + kWsPartialBytes(d->num_sms))
+            return FP8Q_ERR_INVALID_ARG;
+    }
     const int BN = (N % 256 == 0) ? 256 : 128;
     CUtensorMap ta, tb;
     std::memset(&ta, 0, sizeof(ta));
@@ -143,8 +158,14 @@ int gemm_common(const uint8_t* A8, const float* sA, const uint8_t* B8, const flo
     args.K = static_cast<int>(K);
     args.G = G;
     args.status = d->status;
+    args.counters = workspace ? static_cast<int*>(workspace) : nullptr;
+    args.ws = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                    kWsCounterBytes(d->num_sms))
+                        : nullptr;
     const int64_t tiles = (M / 128) * (N / BN);
-    const int tiles_upper = tiles > (int64_t(1) << 30) ? (1 << 30) : static_cast<int>(tiles);
+    // with a workspace every SM takes part (stream-K shares out the tail)
+    const int tiles_upper = workspace ? d->num_sms
+                            : tiles > (int64_t(1) << 30) ? (1 << 30) : static_cast<int>(tiles);
     const bool row_b = bscale == FP8Q_BSCALE_ROW1x128;
     const bool bf16 = out_dtype == FP8Q_BF16;
     return BN == 256 ? launch_gemm_bn<256>(d, ta, tb, args, tiles_upper, row_b, bf16, st)
@@ -217,13 +238,26 @@ int fp8q_quant_w_128x128(const void* w, int in_dtype, int64_t N, int64_t K, uint
 int fp8q_gemm(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB, void* C,
               int64_t M, int64_t N, int64_t K, int out_dtype) {
     return gemm_common(A8, sA, B8, sB, C, nullptr, 1, M, N, K, out_dtype, FP8Q_BSCALE_BLOCK128,
-                       nullptr);
+                       nullptr, 0, nullptr);
 }
 
 int fp8q_gemm_ex(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB, void* C,
                  int64_t M, int64_t N, int64_t K, int out_dtype, int bscale, fp8q_stream_t stream) {
-    return gemm_common(A8, sA, B8, sB, C, nullptr, 1, M, N, K, out_dtype, bscale,
+    return gemm_common(A8, sA, B8, sB, C, nullptr, 1, M, N, K, out_dtype, bscale, nullptr, 0,
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8q_gemm_ws(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB, void* C,
+                 int64_t M, int64_t N, int64_t K, int out_dtype, int bscale, void* workspace,
+                 size_t workspace_bytes, fp8q_stream_t stream) {
+    return gemm_common(A8, sA, B8, sB, C, nullptr, 1, M, N, K, out_dtype, bscale, workspace,
+                       workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t fp8q_gemm_workspace_size(void) {
+    DeviceState* d = nullptr;
+    if (device_state(&d) != FP8Q_OK) return 0;
+    return kWsCounterBytes(d->num_sms) + kWsPartialBytes(d->num_sms);
 }
 
 int fp8q_gemm_grouped(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,
@@ -233,7 +267,19 @@ int fp8q_gemm_grouped(const uint8_t* A8, const float* sA, const uint8_t* B8, con
     if (G < 1 || G > kMaxGroups) return FP8Q_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(m_offsets, 4)) return FP8Q_ERR_MISALIGNED;
     return gemm_common(A8, sA, B8, sB, C, m_offsets, G, M_total, N, K, out_dtype,
-                       FP8Q_BSCALE_BLOCK128, reinterpret_cast<cudaStream_t>(stream));
+                       FP8Q_BSCALE_BLOCK128, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8q_gemm_grouped_ws(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,
+                         void* C, const int* m_offsets, int G, int64_t M_total, int64_t N,
+                         int64_t K, int out_dtype, void* workspace, size_t workspace_bytes,
+                         fp8q_stream_t stream) {
+    if (!m_offsets) return FP8Q_ERR_INVALID_ARG;
+    if (G < 1 || G > kMaxGroups) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(m_offsets, 4)) return FP8Q_ERR_MISALIGNED;
+    return gemm_common(A8, sA, B8, sB, C, m_offsets, G, M_total, N, K, out_dtype,
+                       FP8Q_BSCALE_BLOCK128, workspace, workspace_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fp8q_get_device_status(fp8q_stream_t stream) {

@@ -76,7 +76,8 @@ struct GemmShape {
     static constexpr int kOffBars = kOffScale + kScaleSlots * kSlotBytes;
     static constexpr int kNumBars = 2 * kStages + 2 * kScaleSlots + 5;
     static constexpr int kOffMisc = kOffBars + kNumBars * 8;
-    static constexpr int kOffGroups = kOffMisc + 16;
+    static constexpr int kOffSched = kOffMisc + 32;
+    static constexpr int kOffGroups = kOffSched + 64;
     static constexpr int kSmemBytes = kOffGroups + 2 * (kMaxGroups + 1) * 4 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kTmemCols <= 512, "TMEM budget");
@@ -89,6 +90,91 @@ struct GemmArgs {
     const int* m_offsets;   // grouped: [G+1] device array; dense: nullptr
     int M_total, N, K, G;
     int* status;
+    float* ws;              // stream-K partial tiles, or nullptr (whole tiles only)
+    int* counters;          // stream-K arrival counters, zero between calls
+};
+
+// ------------------------------------------------------------ work schedule
+// Output tiles are numbered t = 0 .. tiles-1, each with Kb K blocks.  With a
+// workspace, the last (partial) wave -- plus one full wave when the partial
+// wave is less than half a wave -- is shared out as "stream-K" work: its tiles' K iterations, laid end to end, are cut into
+// sk_ctas equal contiguous ranges, one per CTA; every other tile is done whole
+// by CTA t % gridDim.x.  A tile cut between CTAs is finished by whichever of
+// them arrives last (per-warp arrival counters): each writes its FP32 partial
+// to the workspace and the last sums all of them in K order, so the result
+// does not depend on arrival order and no CTA ever waits for another.
+struct Sched {
+    int tiles, Kb, G;       // G = gridDim.x
+    int dp_tiles;           // tiles done whole (a multiple of G)
+    int sk_ctas;            // CTAs 0 .. sk_ctas-1 share the stream-K iterations
+    long long sk_iters;     // (tiles - dp_tiles) * Kb
+
+    __device__ void plan(int t_, int kb_, int g_, bool allow_sk) {
+        tiles = t_; Kb = kb_; G = g_;
+        dp_tiles = tiles; sk_ctas = 0; sk_iters = 0;
+        if (!allow_sk || tiles % G == 0) return;
+        const int q = tiles / G, r = tiles % G;
+        const int dp = q == 0 ? 0 : (2 * r >= G ? q * G : (q - 1) * G);
+        const long long S = static_cast<long long>(tiles - dp) * Kb;
+        long long g = S / 8;                   // at least 8 K blocks per CTA (so no
+                                               // stream-K CTA has an empty range)
+        if (g > G) g = G;
+        if (g < 1) g = 1;
+        const long long sk_max = static_cast<long long>(dp / G) * Kb + (S + g - 1) / g;
+        const long long dp_max = static_cast<long long>((tiles + G - 1) / G) * Kb;
+        // a cut tile costs its pieces a partial-tile write, an arrival and
+        // (for the last) the sum: measured at several microseconds, about 16
+        // K blocks of MMA work per CTA
+        if (sk_max + 16 >= dp_max) return;
+        dp_tiles = dp; sk_ctas = static_cast<int>(g); sk_iters = S;
+    }
+    __device__ long long lo(int c) const { return c < sk_ctas ? c * sk_iters / sk_ctas : 0; }
+    __device__ long long hi(int c) const { return c < sk_ctas ? (c + 1) * sk_iters / sk_ctas : 0; }
+    // CTA whose stream-K range holds iteration x.
+    __device__ int cta_of(long long x) const {
+        return static_cast<int>(((x + 1) * sk_ctas - 1) / sk_iters);
+    }
+    // Workspace slot of CTA c's piece of stream-K tile `rel`: each CTA has at
+    // most two split pieces, the first (slot 2c) and the last (2c + 1) of its
+    // range.  Of the CTAs c_lo..c_hi holding pieces of a tile, only c_lo's
+    // piece can be the last of its range (its range starts before the tile).
+    __device__ int slot_in_tile(int c, int c_lo, bool clo_started_before) const {
+        return 2 * c + ((c == c_lo && clo_started_before) ? 1 : 0);
+    }
+};
+
+struct Seg {
+    int t, kb0, kb1;        // tile and its K-block range [kb0, kb1)
+    int rel;                // stream-K tile index (t - dp_tiles) if split, else -1
+    int slot;               // workspace slot of this piece (split pieces only)
+};
+
+struct SegIter {
+    const Sched* sc;
+    int c, t_dp;
+    long long i, end;
+    bool first;             // the next stream-K piece is the first of the range
+    __device__ void start(const Sched* s, int cta) {
+        sc = s; c = cta; t_dp = cta; i = s->lo(cta); end = s->hi(cta); first = true;
+    }
+    __device__ bool next(Seg& g) {
+        if (t_dp < sc->dp_tiles) {
+            g.t = t_dp; g.kb0 = 0; g.kb1 = sc->Kb; g.rel = -1;
+            t_dp += sc->G;
+            return true;
+        }
+        if (i >= end) return false;
+        const int rel = static_cast<int>(i / sc->Kb);
+        const int kb0 = static_cast<int>(i % sc->Kb);
+        const long long left = end - i;
+        const int kb1 = left < sc->Kb - kb0 ? kb0 + static_cast<int>(left) : sc->Kb;
+        g.t = sc->dp_tiles + rel; g.kb0 = kb0; g.kb1 = kb1;
+        g.rel = (kb0 == 0 && kb1 == sc->Kb) ? -1 : rel;
+        g.slot = 2 * c + (first ? 0 : 1);
+        first = false;
+        i += kb1 - kb0;
+        return true;
+    }
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -173,6 +259,7 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + S::kOffMisc);
+    Sched* sched_smem = reinterpret_cast<Sched*>(smem + S::kOffSched);
     int* gtile = reinterpret_cast<int*>(smem + S::kOffGroups);
     int* grow = gtile + (kMaxGroups + 1);
 
@@ -218,6 +305,7 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
             tiles = (args.M_total / kBM) * ntn;
         }
         misc[1] = static_cast<uint32_t>(tiles);
+        sched_smem->plan(tiles, Kb, static_cast<int>(gridDim.x), args.ws != nullptr);
     }
     if (warp == S::kMmaWarp) {
         tmem_alloc(&misc[0], S::kTmemCols);
@@ -231,7 +319,7 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = misc[0];
-    const int num_tiles = static_cast<int>(misc[1]);
+    const Sched& sched = *sched_smem;        // read from shared memory where used
 
     if (warp < S::kFirstPromoWarp) {
         if (S::kRealloc) setmaxnreg_dec<S::kCtrlRegs>();
@@ -239,11 +327,14 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
             // -------------------------------------------------- producer
             uint32_t stage = 0, phase = 0, slot = 0, sphase = 0;
             bool ok = true;
+            SegIter si;
+            si.start(sched_smem, blockIdx.x);
+            Seg sg;
 #pragma unroll 1
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-                const TileCoord tc = decode_tile<BN>(t, grouped, N, args.G, gtile, grow);
+            while (ok && si.next(sg)) {
+                const TileCoord tc = decode_tile<BN>(sg.t, grouped, N, args.G, gtile, grow);
 #pragma unroll 1
-                for (int kb = 0; kb < Kb; ++kb) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, args.status)) { ok = false; break; }
                     uint8_t* sa = smem + stage * S::kStageBytes;
                     mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
@@ -270,10 +361,13 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
             constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
             uint32_t stage = 0, phase = 0, it = 0;
             bool ok = true;
+            SegIter si;
+            si.start(sched_smem, blockIdx.x);
+            Seg sg;
 #pragma unroll 1
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            while (ok && si.next(sg)) {
 #pragma unroll 1
-                for (int kb = 0; kb < Kb; ++kb, ++it) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                     const uint32_t b = it & 1, tph = (it >> 1) & 1;
                     if (!mbar_wait(&tempty[b], tph ^ 1, args.status)) { ok = false; break; }
                     tc_fence_after();
@@ -316,9 +410,13 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
         uint32_t it = 0, slot = 0, sphase = 0;
         bool ok = true;
         float2 acc[64];                            // columns 2j, 2j+1 of this thread's half
+        const int pw = warp - S::kFirstPromoWarp;  // promotion warp: one 32 x 128 slice
+        SegIter si;
+        si.start(sched_smem, blockIdx.x);
+        Seg sg;
 #pragma unroll 1
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-            const TileCoord tc = decode_tile<BN>(t, grouped, N, args.G, gtile, grow);
+        while (ok && si.next(sg)) {
+            const TileCoord tc = decode_tile<BN>(sg.t, grouped, N, args.G, gtile, grow);
             // Block-scaled B: this thread's row scale and the 128x128 block scale
             // are read straight from global memory (coalesced), one block ahead.
             const float* sa_row = args.sA + tc.arow + row;
@@ -326,20 +424,20 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
                 args.sB + (static_cast<size_t>(tc.e) * (N / 128) + (tc.n0 / 128 + half)) * Kb;
             float fa_next = 0.0f, fb_next = 0.0f;
             if (!kRowB) {
-                fa_next = __ldg(sa_row);
-                fb_next = __ldg(sb_blk);
+                fa_next = __ldg(sa_row + static_cast<size_t>(sg.kb0) * args.M_total);
+                fb_next = __ldg(sb_blk + sg.kb0);
             }
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
 #pragma unroll 1
-            for (int kb = 0; kb < Kb; ++kb, ++it) {
+            for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                 const uint32_t b = it & 1, tph = (it >> 1) & 1;
                 float fa, f;
                 const float* sbc = nullptr;
                 if (!kRowB) {
                     fa = fa_next;
                     f = fa_next * fb_next;
-                    if (kb + 1 < Kb) {
+                    if (kb + 1 < sg.kb1) {
                         fa_next = __ldg(sa_row + static_cast<size_t>(kb + 1) * args.M_total);
                         fb_next = __ldg(sb_blk + kb + 1);
                     }
@@ -410,6 +508,55 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
                 }
             }
             if (!ok) break;
+            if (sg.rel >= 0) {
+                // ------------------------------------- stream-K fix-up (per warp)
+                // Partial layout: slot, this warp's slice, column group j (4
+                // floats), row -- so a warp's 32 rows of one group are 512
+                // contiguous bytes.
+                constexpr int kSliceF4 = 32 * 32;          // float4s per 32 x 128 slice
+                float4* mine = reinterpret_cast<float4*>(args.ws) +
+                               (static_cast<size_t>(sg.slot) * S::kPromoWarps + pw) * kSliceF4 + lane;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    __stcg(mine + j * 32, make_float4(acc[2 * j].x, acc[2 * j].y, acc[2 * j + 1].x,
+                                                      acc[2 * j + 1].y));
+                __threadfence();
+                __syncwarp();
+                // pieces of this tile: one for each CTA c_lo .. c_hi
+                const long long tile_start = static_cast<long long>(sg.rel) * Kb;
+                const int c_lo = sched.cta_of(tile_start);
+                const int c_hi = sched.cta_of(tile_start + Kb - 1);
+                const bool clo_before = sched.lo(c_lo) < tile_start;
+                int last = 0;
+                if (lane == 0) {
+                    const int pieces = c_hi - c_lo + 1;
+                    int* cnt = args.counters + static_cast<size_t>(sg.rel) * S::kPromoWarps + pw;
+                    __threadfence();
+                    last = atomicAdd(cnt, 1) == pieces - 1;
+                    if (last) {
+                        *cnt = 0;                           // ready for the next call
+                        __threadfence();
+                    }
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (!last) continue;
+                // the last piece to arrive sums every piece in K order
+#pragma unroll
+                for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
+#pragma unroll 1
+                for (int c = c_lo; c <= c_hi; ++c) {
+                    const float4* src = reinterpret_cast<const float4*>(args.ws) +
+                                        (static_cast<size_t>(sched.slot_in_tile(c, c_lo, clo_before)) * S::kPromoWarps + pw) * kSliceF4 + lane;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float4 v = __ldcg(src + j * 32);
+                        acc[2 * j].x += v.x;
+                        acc[2 * j].y += v.y;
+                        acc[2 * j + 1].x += v.z;
+                        acc[2 * j + 1].y += v.w;
+                    }
+                }
+            }
             // ------------------------------------------------ epilogue
             const size_t crow = static_cast<size_t>(tc.arow + row);
             const int ccol = tc.n0 + half * 128;

@@ -13,9 +13,10 @@
  * Conventions shared by every call
  * --------------------------------
  * - All data pointers are DEVICE pointers owned by the caller; the library
- *   never allocates, frees or keeps them.  Every call is asynchronous on the
- *   given stream (a cudaStream_t; NULL = the legacy default stream) and does
- *   not synchronize.
+ *   never allocates, frees or keeps them (scratch space, where a call can use
+ *   it, is a caller-provided workspace argument).  Every call is asynchronous
+ *   on the given stream (a cudaStream_t; NULL = the legacy default stream)
+ *   and does not synchronize.
  * - Return value: FP8Q_OK or an fp8q_status error code.  Arguments are
  *   checked before anything is launched; on error nothing is launched and
  *   the outputs are untouched.  A failed launch returns FP8Q_ERR_CUDA.
@@ -36,6 +37,7 @@
 #ifndef FP8Q_H
 #define FP8Q_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -140,6 +142,38 @@ FP8Q_API int fp8q_gemm_ex(const uint8_t* A8, const float* sA, const uint8_t* B8,
 FP8Q_API int fp8q_gemm_grouped(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,
                       void* C, const int* m_offsets, int G, int64_t M_total, int64_t N,
                       int64_t K, int out_dtype, fp8q_stream_t stream);
+
+/* Stream-K workspace.  With a workspace, a GEMM runs on every SM and shares
+ * the last partial wave of output tiles (plus one full wave) out by K
+ * iterations, so no SM idles at the end; tiles cut between SMs are finished
+ * through FP32 partial tiles kept in the workspace.  Results do not depend on
+ * the order in which the pieces finish.
+ *
+ * fp8q_gemm_workspace_size: bytes a workspace must have on the CURRENT device
+ * (it depends on the SM count; about 38 MB on a 148-SM B300).  0 on error.
+ *
+ * The workspace is caller-owned device memory, 256-byte aligned.  Its first
+ * 64 * (number of SMs) bytes, rounded up to a multiple of 256, hold arrival
+ * counters that must be ZERO before the first call (simplest: cudaMemset the
+ * whole workspace once); every call that completes leaves them zero again.
+ * After a call that reported a device error, zero them before reusing it.
+ * Calls that may run at the same time (different streams) need different
+ * workspaces. */
+FP8Q_API size_t fp8q_gemm_workspace_size(void);
+
+/* fp8q_gemm_ex with a stream-K workspace (NULL = no workspace: whole tiles
+ * only, exactly as fp8q_gemm_ex).  FP8Q_ERR_INVALID_ARG if workspace_bytes is
+ * smaller than fp8q_gemm_workspace_size(); FP8Q_ERR_MISALIGNED if the
+ * workspace is not 256-byte aligned. */
+FP8Q_API int fp8q_gemm_ws(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,
+                 void* C, int64_t M, int64_t N, int64_t K, int out_dtype, int bscale,
+                 void* workspace, size_t workspace_bytes, fp8q_stream_t stream);
+
+/* fp8q_gemm_grouped with a stream-K workspace (same rules as fp8q_gemm_ws). */
+FP8Q_API int fp8q_gemm_grouped_ws(const uint8_t* A8, const float* sA, const uint8_t* B8,
+                         const float* sB, void* C, const int* m_offsets, int G,
+                         int64_t M_total, int64_t N, int64_t K, int out_dtype, void* workspace,
+                         size_t workspace_bytes, fp8q_stream_t stream);
 
 /* ------------------------------------------------------------------ status */
 
