@@ -17,8 +17,8 @@ __all__ = [
     "Fp8qError", "library_path", "load",
     "fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128",
     "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_gemm_ws", "fp8q_gemm_grouped_ws",
-    "fp8q_gemm_workspace_size", "fp8q_get_device_status", "fp8q_status_string", "fp8q_version",
-    "workspace",
+    "fp8q_gemm_workspace_size", "fp8q_gemm_noalloc", "fp8q_get_device_status",
+    "fp8q_status_string", "fp8q_version", "workspace",
     "quant_act_1x128", "quant_act_128x1", "quant_w_128x128", "gemm", "gemm_grouped",
     "F32", "BF16", "BSCALE_BLOCK128", "BSCALE_ROW1x128",
 ]
@@ -33,8 +33,8 @@ STATUS_NAMES = {0: "FP8Q_OK", 1: "FP8Q_ERR_INVALID_ARG", 2: "FP8Q_ERR_UNSUPPORTE
                 6: "FP8Q_ERR_BAD_GROUPS"}
 EXPORTS = ("fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128", "fp8q_gemm",
            "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_gemm_ws", "fp8q_gemm_grouped_ws",
-           "fp8q_gemm_workspace_size", "fp8q_get_device_status", "fp8q_status_string",
-           "fp8q_version")
+           "fp8q_gemm_workspace_size", "fp8q_gemm_noalloc", "fp8q_get_device_status",
+           "fp8q_status_string", "fp8q_version")
 
 
 class Fp8qError(RuntimeError):
@@ -77,6 +77,8 @@ def load():
     lib.fp8q_gemm_grouped_ws.restype = I
     lib.fp8q_gemm_workspace_size.argtypes = []
     lib.fp8q_gemm_workspace_size.restype = SZ
+    lib.fp8q_gemm_noalloc.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, P]
+    lib.fp8q_gemm_noalloc.restype = I
     lib.fp8q_get_device_status.argtypes = [P]
     lib.fp8q_get_device_status.restype = I
     lib.fp8q_status_string.argtypes = [I]
@@ -203,6 +205,16 @@ def fp8q_gemm_grouped_ws(A8, sA, B8, sB, C, m_offsets, ws=None, stream=None):
         _dev(A8, "A8", torch.uint8), _dev(sA, "sA", torch.float32), _dev(B8, "B8", torch.uint8),
         _dev(sB, "sB", torch.float32), _dev(C, "C"), _dev(m_offsets, "m_offsets", torch.int32),
         G, Mtot, N, K, _out_dtype(C.dtype), wp, wn, _stream(stream)))
+
+
+def fp8q_gemm_noalloc(A8, sA, B8, sB, C, bscale=BSCALE_BLOCK128, stream=None):
+    """The stream-K GEMM on the library's own scratch array (no allocation)."""
+    M, K = A8.shape
+    N = B8.shape[0]
+    _check("fp8q_gemm_noalloc", load().fp8q_gemm_noalloc(
+        _dev(A8, "A8", torch.uint8), _dev(sA, "sA", torch.float32), _dev(B8, "B8", torch.uint8),
+        _dev(sB, "sB", torch.float32), _dev(C, "C"), M, N, K, _out_dtype(C.dtype), int(bscale),
+        _stream(stream)))
 
 
 def fp8q_gemm_workspace_size() -> int:

@@ -18,6 +18,15 @@ namespace fp8q {
 
 __device__ int g_status;   // sticky device-side status, one per device
 
+// Scratch of fp8q_gemm_noalloc: the stream-K workspace kept inside the library
+// for callers that cannot allocate device memory.  40 MiB fits the workspace
+// of a GPU with up to 159 SMs (37.9 MB on a 148-SM B300).  It is zero when the
+// library is loaded and every device that loads the library holds it until
+// the process exits.  In host code the name is only a handle: the device
+// address comes from cudaGetSymbolAddress (see device_state).
+constexpr size_t kNoAllocScratchBytes = size_t(40) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -27,6 +36,7 @@ struct DeviceState {
     int num_sms = 0;
     int* status = nullptr;            // device address of g_status on this device
     bool gemm_attr[2][2][2] = {};     // dynamic-smem attribute set, per kernel instance
+    uint8_t* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch
 };
 
 std::mutex g_mutex;
@@ -53,6 +63,9 @@ int device_state(DeviceState** out) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return cuda_fail();
         d.status = static_cast<int*>(p);
+        void* sp = nullptr;
+        if (cudaGetSymbolAddress(&sp, g_noalloc_scratch) != cudaSuccess) return cuda_fail();
+        d.noalloc_scratch = static_cast<uint8_t*>(sp);
         if (!g_encode) {
             cudaDriverEntryPointQueryResult q;
             void* fn = nullptr;
@@ -268,6 +281,35 @@ int fp8q_gemm_grouped(const uint8_t* A8, const float* sA, const uint8_t* B8, con
     if (!aligned(m_offsets, 4)) return FP8Q_ERR_MISALIGNED;
     return gemm_common(A8, sA, B8, sB, C, m_offsets, G, M_total, N, K, out_dtype,
                        FP8Q_BSCALE_BLOCK128, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8q_gemm_noalloc(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,
+                      void* C, int64_t M, int64_t N, int64_t K, int out_dtype, int bscale,
+                      fp8q_stream_t stream) {
+    // the same argument checks as the workspace GEMM, made before the counter
+    // clear below is launched (nothing is launched when they fail)
+    if (!A8 || !sA || !B8 || !sB || !C) return FP8Q_ERR_INVALID_ARG;
+    if (out_dtype != FP8Q_F32 && out_dtype != FP8Q_BF16) return FP8Q_ERR_INVALID_ARG;
+    if (bscale != FP8Q_BSCALE_BLOCK128 && bscale != FP8Q_BSCALE_ROW1x128) return FP8Q_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0) return FP8Q_ERR_INVALID_ARG;
+    if (M % 128 || N % 128 || K % 128) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (M > (int64_t(1) << 30) || N > (int64_t(1) << 24) || K > (int64_t(1) << 30))
+        return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(A8, 16) || !aligned(B8, 16) || !aligned(sA, 16) || !aligned(C, 16))
+        return FP8Q_ERR_MISALIGNED;
+    if (!aligned(sB, bscale == FP8Q_BSCALE_ROW1x128 ? 16 : 4)) return FP8Q_ERR_MISALIGNED;
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != FP8Q_OK) return rc;
+    const size_t counters = kWsCounterBytes(d->num_sms);
+    const size_t need = counters + kWsPartialBytes(d->num_sms);
+    if (need > kNoAllocScratchBytes) return FP8Q_ERR_UNSUPPORTED_SHAPE;   // more SMs than it fits
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the arrival counters must start at zero; a call that failed on the
+    // device may have left some set, so clear them every time
+    if (cudaMemsetAsync(d->noalloc_scratch, 0, counters, st) != cudaSuccess) return cuda_fail();
+    return gemm_common(A8, sA, B8, sB, C, nullptr, 1, M, N, K, out_dtype, bscale,
+                       d->noalloc_scratch, kNoAllocScratchBytes, st);
 }
 
 int fp8q_gemm_grouped_ws(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,

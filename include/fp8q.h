@@ -175,6 +175,31 @@ FP8Q_API int fp8q_gemm_grouped_ws(const uint8_t* A8, const float* sA, const uint
                          int64_t M_total, int64_t N, int64_t K, int out_dtype, void* workspace,
                          size_t workspace_bytes, fp8q_stream_t stream);
 
+/* fp8q_gemm_ws without a caller workspace, for callers that cannot allocate
+ * device memory: code that must not call cudaMalloc while a CUDA graph is
+ * being captured, or that runs inside a framework or plugin whose memory is
+ * handed out by someone else (a fixed budget, a caching allocator it cannot
+ * reach), or that simply has no allocator of its own.  No counterpart on the
+ * pages: this is an engineering convenience of the library, not part of the
+ * method.
+ *
+ * The stream-K workspace lives in a 40 MiB array inside the library, held by
+ * every GPU that loads the library until the process exits.  That is enough
+ * for a GPU with up to 159 SMs; on a larger GPU the call returns
+ * FP8Q_ERR_UNSUPPORTED_SHAPE and launches nothing.  The call allocates
+ * nothing (no cudaMalloc, no cudaFree, no allocating library routine).  It
+ * clears the array's arrival counters (an asynchronous memset on `stream`)
+ * and then runs exactly as fp8q_gemm_ws.
+ *
+ * Every call shares the one array per device: calls that may overlap on the
+ * GPU (different streams, or host threads, without ordering between them)
+ * race and must not be made.  The array's device address is looked up the
+ * first time the library is used on a device; make that first call (of any
+ * fp8q function) before starting a stream capture. */
+FP8Q_API int fp8q_gemm_noalloc(const uint8_t* A8, const float* sA, const uint8_t* B8,
+                      const float* sB, void* C, int64_t M, int64_t N, int64_t K, int out_dtype,
+                      int bscale, fp8q_stream_t stream);
+
 /* ------------------------------------------------------------------ status */
 
 /* Synchronizes `stream`, returns the sticky device status of the current
