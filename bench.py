@@ -53,8 +53,9 @@ def measured_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the GEMM kernel sources the committed DRAM-traffic figures were taken on."""
     h = hashlib.sha256()
-    for f in ("gemm.cuh", "ptx.cuh", "quant.cuh", "fp8q.cu"):
+    for f in ("gemm.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "fp8_fine_grained_21_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -63,7 +64,7 @@ def kernel_source_hash():
 def profiled_traffic(kernel_key):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    path = os.path.join(ROOT, "profiles", "k_gemm_dram_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
@@ -88,7 +89,7 @@ class ClockSampler:
         except Exception:
             sel = []
         self.cmd = ["nvidia-smi", *sel, "--query-gpu=" + self.FIELDS,
-                    "--format=csv,noheader,nounits", "-lms", "50"]
+                    "--format=csv,noheader,nounits", "-lms", "20"]
 
     def start(self):
         try:
@@ -474,7 +475,11 @@ def run_fp8q(args):
                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                       "ms_per_step": e2e_ms}
     if world == 1 and not args.no_cpu_baseline:
-        cb = oracle_sample(args.workload, 256, data=wl.host)
+        # size the oracle's sample to about 12 s of CPU work (cost ~ rows^2)
+        probe = oracle_sample(args.workload, 128, data=wl.host)
+        rows = int(128 * (12.0 / max(probe["sample_s"], 1e-3)) ** 0.5) // 128 * 128
+        rows = max(128, min(rows, wl.M, wl.N))
+        cb = oracle_sample(args.workload, rows, data=wl.host)
         out["cpu_baseline"] = {"value": cb["tflops"], "unit": "TFLOPS", "cores": cb["cores"],
                                "kind": "oracle", "sample": cb["sample"],
                                "sample_seconds": cb["sample_s"]}
