@@ -18,7 +18,7 @@ __all__ = [
     "fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128",
     "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_gemm_ws", "fp8q_gemm_grouped_ws",
     "fp8q_gemm_workspace_size", "fp8q_gemm_noalloc", "fp8q_get_device_status",
-    "fp8q_status_string", "fp8q_version", "workspace",
+    "fp8q_selftest_wait", "fp8q_status_string", "fp8q_version", "workspace",
     "quant_act_1x128", "quant_act_128x1", "quant_w_128x128", "gemm", "gemm_grouped",
     "F32", "BF16", "BSCALE_BLOCK128", "BSCALE_ROW1x128",
 ]
@@ -34,7 +34,7 @@ STATUS_NAMES = {0: "FP8Q_OK", 1: "FP8Q_ERR_INVALID_ARG", 2: "FP8Q_ERR_UNSUPPORTE
 EXPORTS = ("fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128", "fp8q_gemm",
            "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_gemm_ws", "fp8q_gemm_grouped_ws",
            "fp8q_gemm_workspace_size", "fp8q_gemm_noalloc", "fp8q_get_device_status",
-           "fp8q_status_string", "fp8q_version")
+           "fp8q_selftest_wait", "fp8q_status_string", "fp8q_version")
 
 
 class Fp8qError(RuntimeError):
@@ -79,6 +79,8 @@ def load():
     lib.fp8q_gemm_workspace_size.restype = SZ
     lib.fp8q_gemm_noalloc.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, P]
     lib.fp8q_gemm_noalloc.restype = I
+    lib.fp8q_selftest_wait.argtypes = [I64, P]
+    lib.fp8q_selftest_wait.restype = I
     lib.fp8q_get_device_status.argtypes = [P]
     lib.fp8q_get_device_status.restype = I
     lib.fp8q_status_string.argtypes = [I]
@@ -244,6 +246,10 @@ def workspace(device=None, stream=None):
 
 def fp8q_get_device_status(stream=None) -> int:
     return int(load().fp8q_get_device_status(_stream(stream)))
+
+
+def fp8q_selftest_wait(limit_ns: int, stream=None):
+    _check("fp8q_selftest_wait", load().fp8q_selftest_wait(int(limit_ns), _stream(stream)))
 
 
 def fp8q_status_string(status: int) -> str:

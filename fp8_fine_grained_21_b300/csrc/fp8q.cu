@@ -27,6 +27,20 @@ __device__ int g_status;   // sticky device-side status, one per device
 constexpr size_t kNoAllocScratchBytes = size_t(40) << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
+// Diagnostic for the bounded waits: one warp waits on an mbarrier that nothing
+// arrives on, through the same wait the GEMM pipeline uses, so the wait runs
+// out after limit_ns and records kErrTimeout; the kernel then returns.
+__global__ void k_selftest_wait(int* status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const bool done = mbar_wait_for(&bar, 0, status, limit_ns);
+    (void)done;
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -241,10 +255,10 @@ int fp8q_quant_w_128x128(const void* w, int in_dtype, int64_t N, int64_t K, uint
     const dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (in_dtype == FP8Q_BF16)
-        k_quant_128x128<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w), N,
+        k_quant_128x128<__nv_bfloat16><<<grid, kQwThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(w), N,
                                                              K, q, s);
     else
-        k_quant_128x128<float><<<grid, 256, 0, st>>>(static_cast<const float*>(w), N, K, q, s);
+        k_quant_128x128<float><<<grid, kQwThreads, 0, st>>>(static_cast<const float*>(w), N, K, q, s);
     return launched();
 }
 
@@ -339,6 +353,16 @@ int fp8q_get_device_status(fp8q_stream_t stream) {
             return cuda_fail();
     }
     return v;
+}
+
+int fp8q_selftest_wait(int64_t limit_ns, fp8q_stream_t stream) {
+    if (limit_ns <= 0 || limit_ns > 100000000) return FP8Q_ERR_INVALID_ARG;
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != FP8Q_OK) return rc;
+    k_selftest_wait<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        d->status, static_cast<uint64_t>(limit_ns));
+    return launched();
 }
 
 const char* fp8q_status_string(int status) {

@@ -67,9 +67,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
-// (returning false) when the time limit passes or when another thread has
+// (returning false) when `limit_ns` passes or when another thread has
 // already recorded a failure in *status; a timeout records kErrTimeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, int* status,
+                                              uint64_t limit_ns) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -78,11 +79,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
         for (int i = 0; i < 256; ++i)
             if (mbar_try_wait(a, parity)) return true;
         if (*reinterpret_cast<volatile int*>(status) != kOk) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             atomicCAS(status, kOk, kErrTimeout);
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+    return mbar_wait_for(bar, parity, status, kWaitLimitNs);
 }
 
 // Named barrier 1 over the whole CTA (usable from different code locations).

@@ -76,22 +76,30 @@ __device__ __forceinline__ uint2 quant8(const float (&v)[8], float inv) {
 }
 
 // ------------------------------------------------------------------ 1x128
-// Grid (K/128, ceil(M/64)), 256 threads.  A half-warp (16 lanes x 8 elements)
-// covers one 1x128 tile; each thread handles 4 rows 16 apart, issuing all 4
-// loads before reducing.  Scales land at s[g*M + m].
-constexpr int kQ1Rows = 64;
+// Grid (K/128, ceil(M / (16 * kRows))), 256 threads.  A half-warp (16 lanes
+// x 8 elements) covers one 1x128 tile; each thread handles kRows rows 16
+// apart, issuing all kRows loads before reducing.  Scales land at s[g*M + m].
+#ifndef FP8Q_Q1_ROWS
+#define FP8Q_Q1_ROWS 4
+#endif
+#ifndef FP8Q_Q1_MINB
+#define FP8Q_Q1_MINB 6
+#endif
+constexpr int kQ1RowsPerThread = FP8Q_Q1_ROWS;
+constexpr int kQ1Rows = 16 * kQ1RowsPerThread;
 
 template <typename T>
-__global__ void __launch_bounds__(256) k_quant_1x128(const T* __restrict__ x, int64_t M, int64_t K,
-                                                     uint8_t* __restrict__ q,
-                                                     float* __restrict__ s) {
+__global__ void __launch_bounds__(256, FP8Q_Q1_MINB) k_quant_1x128(const T* __restrict__ x, int64_t M,
+                                                                  int64_t K, uint8_t* __restrict__ q,
+                                                                  float* __restrict__ s) {
+    constexpr int R = kQ1RowsPerThread;
     const int64_t g = blockIdx.x;
     const int team = threadIdx.x >> 4, tl = threadIdx.x & 15;
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kQ1Rows + team;
     const int64_t col = g * 128 + tl * 8;
-    float v[4][8];
+    float v[R][8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < R; ++i) {
         const int64_t r = r0 + 16 * i;
         if (r < M) {
             load8(x + r * K + col, v[i]);
@@ -101,7 +109,7 @@ __global__ void __launch_bounds__(256) k_quant_1x128(const T* __restrict__ x, in
         }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < R; ++i) {
         float a = amax8(v[i]);
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
@@ -118,37 +126,48 @@ __global__ void __launch_bounds__(256) k_quant_1x128(const T* __restrict__ x, in
 }
 
 // ---------------------------------------------------------------- 128x128
-// Grid (K/128, N/128), 256 threads, one block per CTA.  Thread (r0, tl)
-// holds rows r0 + 16 i (i < 8), 8 columns each, in registers from the load
-// to the store; block amax via warp shuffles and a shared-memory step.
+// Grid (K/128, N/128), kQwThreads threads, one block per CTA.  Thread (rr, tl)
+// holds rows rr + (kQwThreads/16) i of the block, 8 columns each, in
+// registers from the load to the store; block amax via warp shuffles and a
+// shared-memory step.
+#ifndef FP8Q_QW_THREADS
+#define FP8Q_QW_THREADS 256
+#endif
+#ifndef FP8Q_QW_MINB
+#define FP8Q_QW_MINB 1
+#endif
+constexpr int kQwThreads = FP8Q_QW_THREADS;
+
 template <typename T>
-__global__ void __launch_bounds__(256) k_quant_128x128(const T* __restrict__ w, int64_t N, int64_t K,
-                                                       uint8_t* __restrict__ q,
-                                                       float* __restrict__ s) {
-    __shared__ float red[8];
+__global__ void __launch_bounds__(kQwThreads, FP8Q_QW_MINB) k_quant_128x128(const T* __restrict__ w,
+                                                                           int64_t N, int64_t K,
+                                                                           uint8_t* __restrict__ q,
+                                                                           float* __restrict__ s) {
+    constexpr int kWarps = kQwThreads / 32, kStride = kQwThreads / 16, R = 128 / kStride;
+    __shared__ float red[kWarps];
     const int64_t g = blockIdx.x, nb = blockIdx.y;
     const int64_t Kb = gridDim.x;
     const int tl = threadIdx.x & 15, rr = threadIdx.x >> 4;
     const int64_t col = g * 128 + tl * 8;
-    float v[8][8];
+    float v[R][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) load8(w + (nb * 128 + rr + 16 * i) * K + col, v[i]);
+    for (int i = 0; i < R; ++i) load8(w + (nb * 128 + rr + kStride * i) * K + col, v[i]);
     float a = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) a = fmaxf(a, amax8(v[i]));
+    for (int i = 0; i < R; ++i) a = fmaxf(a, amax8(v[i]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
     __syncthreads();
     a = red[0];
 #pragma unroll
-    for (int i = 1; i < 8; ++i) a = fmaxf(a, red[i]);
+    for (int i = 1; i < kWarps; ++i) a = fmaxf(a, red[i]);
     float sc, inv;
     group_scale(a, sc, inv);
     if (threadIdx.x == 0) s[nb * Kb + g] = sc;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        *reinterpret_cast<uint2*>(q + (nb * 128 + rr + 16 * i) * K + col) = quant8(v[i], inv);
+    for (int i = 0; i < R; ++i)
+        *reinterpret_cast<uint2*>(q + (nb * 128 + rr + kStride * i) * K + col) = quant8(v[i], inv);
 }
 
 // ------------------------------------------------------------------ 128x1

@@ -206,6 +206,15 @@ FP8Q_API int fp8q_gemm_noalloc(const uint8_t* A8, const float* sA, const uint8_t
  * device (FP8Q_OK if no kernel recorded a problem) and clears it. */
 FP8Q_API int fp8q_get_device_status(fp8q_stream_t stream);
 
+/* Diagnostic of the device-side failure detection: launches one warp that
+ * waits on a barrier nothing arrives on, through the bounded wait every GEMM
+ * pipeline stage uses, with a time limit of limit_ns (1 .. 100,000,000 ns).
+ * The wait runs out, FP8Q_ERR_TIMEOUT is recorded in the sticky device
+ * status (read it with fp8q_get_device_status), and the kernel returns: the
+ * GPU and the CUDA context stay usable.  FP8Q_ERR_INVALID_ARG for a limit out
+ * of range.  Not part of the method; used by the library's tests. */
+FP8Q_API int fp8q_selftest_wait(int64_t limit_ns, fp8q_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 FP8Q_API const char* fp8q_status_string(int status);
 

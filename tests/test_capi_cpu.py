@@ -94,6 +94,26 @@ def test_gemm_argument_checks(lib):
     assert gg(*ok, P(0x10002), 4, 512, 128, 128, 1, None) == 3  # misaligned offsets
 
 
+def test_workspace_and_noalloc_argument_checks(lib):
+    ok = (A16, A16b, A16c, P(0x40000), P(0x50000))
+    w = lib.fp8q_gemm_ws
+    assert w(None, *ok[1:], 128, 128, 128, 0, 0, A16, 1 << 30, None) == 1
+    assert w(*ok, 128, 128, 64, 0, 0, A16, 1 << 30, None) == 2          # ragged K
+    na = lib.fp8q_gemm_noalloc
+    assert na(None, *ok[1:], 128, 128, 128, 0, 0, None) == 1
+    assert na(*ok, 128, 128, 128, 5, 0, None) == 1                       # bad out dtype
+    assert na(*ok, 128, 136, 128, 0, 0, None) == 2                       # ragged N
+    assert na(MIS, *ok[1:], 128, 128, 128, 0, 0, None) == 3
+    gw = lib.fp8q_gemm_grouped_ws
+    assert gw(*ok, None, 4, 512, 128, 128, 1, A16, 1 << 30, None) == 1
+
+
+def test_selftest_wait_limit_checks(lib):
+    assert lib.fp8q_selftest_wait(0, None) == 1
+    assert lib.fp8q_selftest_wait(-5, None) == 1
+    assert lib.fp8q_selftest_wait(100000001, None) == 1
+
+
 def test_python_binding_refuses_cpu_tensors(lib):
     import torch
 
