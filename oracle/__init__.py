@@ -44,6 +44,7 @@ def _load():
         lib.fpo_tile_scale.argtypes = [ctypes.c_float, P, P]
         for name in ("fpo_quant_1x128", "fpo_quant_128x1", "fpo_quant_128x128"):
             getattr(lib, name).argtypes = [P, I64, I64, P, P]
+        lib.fpo_retile_1x128_to_128x1.argtypes = [P, P, I64, I64, P, P]
         lib.fpo_gemm_f64.argtypes = [P, P, P, P, I, I64, I64, I64, P, P, I]
         lib.fpo_gemm_f64_entries.argtypes = [P, P, P, P, I, I64, I64, I64, P, P, I64, P, P, I]
         lib.fpo_gemm_grouped_f64.argtypes = [P, P, P, P, P, I64, I64, I64, I64, P, P, I]
@@ -138,6 +139,26 @@ def quant_128x128(w):
     s = np.empty((_nb(N), _nb(K)), np.float32)
     _load().fpo_quant_128x128(_ptr(w), N, K, _ptr(q), _ptr(s))
     return q, s
+
+
+def retile_1x128_to_128x1(q, s):
+    """Backward regrouping of stored forward tiles ("Six Reasons...", para. 3):
+    dequantize q[T][C] (1x128 scales s[ceil(C/128)][T]) and quantize per 128
+    tokens of a channel, transposed: -> qT[C][T], sT[ceil(T/128)][C]."""
+    q = _c(q, np.uint8)
+    s = _c(s, np.float32)
+    T, C = q.shape
+    qT = np.empty((C, T), np.uint8)
+    sT = np.empty((_nb(T), C), np.float32)
+    _load().fpo_retile_1x128_to_128x1(_ptr(q), _ptr(s), T, C, _ptr(qT), _ptr(sT))
+    return qT, sT
+
+
+def dequant_1x128(q, s):
+    """decode(q) * s per element, in FP64 (exact: both factors are FP32-exact)."""
+    q = _c(q, np.uint8)
+    M, K = q.shape
+    return e4m3_decode(q) * np.repeat(np.asarray(s, np.float64).T, GROUP, axis=1)[:, :K]
 
 
 # ------------------------------------------------------------------- GEMM

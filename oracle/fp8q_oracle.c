@@ -220,6 +220,29 @@ void fpo_quant_128x128(const float* w, int64_t N, int64_t K, uint8_t* q, float* 
     }
 }
 
+/* [P1] para. 3: in the backward pass the activations are converted from 1x128
+ * tiles to 128x1 tiles; with the forward pass's quantized activations stored
+ * as 1x128 FP8 tiles ([P2] para. 4), the conversion starts from those tiles.
+ * Each stored element is dequantized -- decode(q) * s, the decode exact in
+ * float and the product one correctly rounded FP32 multiplication -- and the
+ * dequantized tensor is quantized per 128 tokens of one channel exactly as
+ * fpo_quant_128x1 does, written transposed.
+ * q[T][C], s[ceil(C/128)][T] -> qT[C][T], sT[ceil(T/128)][C]. */
+void fpo_retile_1x128_to_128x1(const uint8_t* q, const float* s, int64_t T, int64_t C,
+                               uint8_t* qT, float* sT)
+{
+    float* x = (float*)malloc((size_t)(T * C) * sizeof(float));
+    if (!x)
+        return;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < C; ++c) {
+            float d = (float)fpo_e4m3_decode(q[t * C + c]);
+            x[t * C + c] = d * s[(c / FPO_GROUP) * T + t];
+        }
+    fpo_quant_128x1(x, T, C, qT, sT);
+    free(x);
+}
+
 /* ------------------------------------------------------------------- GEMM */
 
 /* Scale of operand B for output column n and K group g.
