@@ -136,6 +136,9 @@ def describe(name):
         "accum": "accum: A[1024][16384] x B[1024][16384] bf16 U(-1,1), 1x128 / 128x128 -> f32",
         "grouped": "grouped: 32 experts (Multinomial(16384, Zipf 1.1), M_e rounded up to 128), "
                    "N=2048, K=7168, bf16 -> bf16",
+        "backward": "backward data path of forward: dY[4096][2048] bf16 1x128-quantized, stored "
+                    "W8[2048][7168] transposed, stored A8 tiles regrouped 1x128 -> 128x1, "
+                    "dX[4096][7168] = dY W -> bf16",
     }[name]
 
 
@@ -164,6 +167,12 @@ class Workload:
             self.K = T
             self.inputs_host = [dY, X]
             self.out_dtype = torch.float32
+        elif name == "backward":
+            self.M, self.N = d["dY"].shape[0], d["W"].shape[1]
+            self.K = d["dY"].shape[1]
+            self.inputs_host = [d["dY"], d["A"], d["W"]]
+            self.out_dtype = torch.bfloat16
+            self.launches_per_step = 4
         elif name == "grouped":
             A, W, offs = d["A"], d["W"], d["m_offsets"]
             self.G, self.N, self.K = W.shape
@@ -176,8 +185,17 @@ class Workload:
         self.desc = describe(name)
         self.inputs = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).to(device)
                        for h in self.inputs_host]
-        x0, x1 = self.inputs
-        if name == "wgrad":
+        x0, x1 = self.inputs[:2]
+        if name == "backward":
+            # the forward pass's stored FP8 tiles (set-up, not part of the step)
+            self.af8, self.saf = fq.quant_act_1x128(self.inputs[1])
+            self.wf8, self.swf = fq.quant_w_128x128(self.inputs[2])
+            self.inputs = self.inputs[:1]                 # the step's only new input is dY
+            self.inputs_host = self.inputs_host[:1]
+            self.a8, self.sa = fq.quant_act_1x128(x0)      # dY 1x128 (inner dim N = 2048)
+            self.b8, self.sb = fq.transpose_w_128x128(self.wf8, self.swf)
+            self.at8, self.sat = fq.retile_1x128_to_128x1(self.af8, self.saf)
+        elif name == "wgrad":
             self.a8, self.sa = fq.quant_act_128x1(x0)
             self.b8, self.sb = fq.quant_act_128x1(x1)
         else:
@@ -190,7 +208,12 @@ class Workload:
         self.flops = 2.0 * self.M * self.N * self.K
         e0, e1 = x0.numel(), x1.numel()
         # algorithmic bytes: BF16 in + FP8 out + FP32 scales
-        if name == "wgrad":
+        if name == "backward":
+            ew, ea = self.wf8.numel(), self.af8.numel()
+            # dY quantization; weight transpose + activation regrouping (side stream)
+            self.quant_bytes = [e0 * 3 + e0 * 4 // 128,
+                                (2 * ew + 8 * ew // 16384) + (2 * ea + 2 * (ea * 4 // 128))]
+        elif name == "wgrad":
             self.quant_bytes = [e0 * 3 + e0 * 4 // 128, e1 * 3 + e1 * 4 // 128]
         else:
             self.quant_bytes = [e0 * 3 + e0 * 4 // 128, e1 * 3 + e1 * 4 // 16384]
@@ -199,14 +222,19 @@ class Workload:
 
     def quant0(self, stream=None):
         fq = self.fq
-        if self.name == "wgrad":
+        if self.name == "backward":
+            fq.fp8q_quant_act_1x128(self.inputs[0], self.a8, self.sa, stream)
+        elif self.name == "wgrad":
             fq.fp8q_quant_act_128x1(self.inputs[0], self.a8, self.sa, stream)
         else:
             fq.fp8q_quant_act_1x128(self.inputs[0], self.a8, self.sa, stream)
 
     def quant1(self, stream=None):
         fq = self.fq
-        if self.name == "wgrad":
+        if self.name == "backward":
+            fq.fp8q_transpose_w_128x128(self.wf8, self.swf, self.b8, self.sb, stream)
+            fq.fp8q_retile_1x128_to_128x1(self.af8, self.saf, self.at8, self.sat, stream)
+        elif self.name == "wgrad":
             fq.fp8q_quant_act_128x1(self.inputs[1], self.b8, self.sb, stream)
         else:
             fq.fp8q_quant_w_128x128(self.inputs[1], self.b8, self.sb, stream)
@@ -327,6 +355,11 @@ def oracle_sample(name, rows, kcols=None, seed=0, threads=0, data=None):
             M, K = A.shape
             N = d["W"].shape[1]
             full_elems = A.size + d["W"].size
+        elif name == "backward":
+            A, B = d["dY"], np.ascontiguousarray(d["W"].T)   # dX = dY (W^T)^T
+            M, K = A.shape
+            N = B.shape[0]
+            full_elems = A.size + d["A"].size + d["W"].size
         else:
             A, B = (d["A"], d["W"]) if name == "forward" else (d["A"], d["B"])
             M, K = A.shape
@@ -503,7 +536,7 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["fp8q", "reference"], default="fp8q")
-    ap.add_argument("--workload", choices=["forward", "wgrad", "accum", "grouped"],
+    ap.add_argument("--workload", choices=["forward", "wgrad", "accum", "grouped", "backward"],
                     default="forward")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -16,6 +16,8 @@ import torch
 __all__ = [
     "Fp8qError", "library_path", "load",
     "fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128",
+    "fp8q_retile_1x128_to_128x1", "fp8q_transpose_w_128x128", "retile_1x128_to_128x1",
+    "transpose_w_128x128",
     "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_gemm_ws", "fp8q_gemm_grouped_ws",
     "fp8q_gemm_workspace_size", "fp8q_gemm_noalloc", "fp8q_get_device_status",
     "fp8q_selftest_wait", "fp8q_status_string", "fp8q_version", "workspace",
@@ -31,7 +33,8 @@ BSCALE_BLOCK128, BSCALE_ROW1x128 = 0, 1
 STATUS_NAMES = {0: "FP8Q_OK", 1: "FP8Q_ERR_INVALID_ARG", 2: "FP8Q_ERR_UNSUPPORTED_SHAPE",
                 3: "FP8Q_ERR_MISALIGNED", 4: "FP8Q_ERR_CUDA", 5: "FP8Q_ERR_TIMEOUT",
                 6: "FP8Q_ERR_BAD_GROUPS"}
-EXPORTS = ("fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128", "fp8q_gemm",
+EXPORTS = ("fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128",
+           "fp8q_retile_1x128_to_128x1", "fp8q_transpose_w_128x128", "fp8q_gemm",
            "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_gemm_ws", "fp8q_gemm_grouped_ws",
            "fp8q_gemm_workspace_size", "fp8q_gemm_noalloc", "fp8q_get_device_status",
            "fp8q_selftest_wait", "fp8q_status_string", "fp8q_version")
@@ -63,6 +66,10 @@ def load():
     for name in ("fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128"):
         f = getattr(lib, name)
         f.argtypes = [P, I, I64, I64, P, P, P]
+        f.restype = I
+    for name in ("fp8q_retile_1x128_to_128x1", "fp8q_transpose_w_128x128"):
+        f = getattr(lib, name)
+        f.argtypes = [P, P, I64, I64, P, P, P]
         f.restype = I
     lib.fp8q_gemm.argtypes = [P, P, P, P, P, I64, I64, I64, I]
     lib.fp8q_gemm.restype = I
@@ -155,6 +162,20 @@ def fp8q_quant_w_128x128(w, q, s, stream=None):
     _check("fp8q_quant_w_128x128", load().fp8q_quant_w_128x128(
         _dev(w, "w"), _in_dtype(w), N, K, _dev(q, "q", torch.uint8),
         _dev(s, "s", torch.float32), _stream(stream)))
+
+
+def fp8q_retile_1x128_to_128x1(q, s, qT, sT, stream=None):
+    T, C = q.shape
+    _check("fp8q_retile_1x128_to_128x1", load().fp8q_retile_1x128_to_128x1(
+        _dev(q, "q", torch.uint8), _dev(s, "s", torch.float32), T, C, _dev(qT, "qT", torch.uint8),
+        _dev(sT, "sT", torch.float32), _stream(stream)))
+
+
+def fp8q_transpose_w_128x128(q, s, qT, sT, stream=None):
+    N, K = q.shape
+    _check("fp8q_transpose_w_128x128", load().fp8q_transpose_w_128x128(
+        _dev(q, "q", torch.uint8), _dev(s, "s", torch.float32), N, K, _dev(qT, "qT", torch.uint8),
+        _dev(sT, "sT", torch.float32), _stream(stream)))
 
 
 def fp8q_gemm(A8, sA, B8, sB, C):
@@ -290,6 +311,24 @@ def quant_w_128x128(w, stream=None):
     s = torch.empty((_scales(N), _scales(K)), dtype=torch.float32, device=w.device)
     fp8q_quant_w_128x128(w, q, s, stream)
     return q, s
+
+
+def retile_1x128_to_128x1(q, s, stream=None):
+    """Stored 1x128 tiles q[T][C] (scales s[C/128][T]) -> (qT[C][T], sT[T/128][C])."""
+    T, C = q.shape
+    qT = torch.empty((C, T), dtype=torch.uint8, device=q.device)
+    sT = torch.empty((_scales(T), C), dtype=torch.float32, device=q.device)
+    fp8q_retile_1x128_to_128x1(q, s, qT, sT, stream)
+    return qT, sT
+
+
+def transpose_w_128x128(q, s, stream=None):
+    """q[N][K], s[N/128][K/128] -> (qT[K][N], sT[K/128][N/128])."""
+    N, K = q.shape
+    qT = torch.empty((K, N), dtype=torch.uint8, device=q.device)
+    sT = torch.empty((_scales(K), _scales(N)), dtype=torch.float32, device=q.device)
+    fp8q_transpose_w_128x128(q, s, qT, sT, stream)
+    return qT, sT
 
 
 def gemm(A8, sA, B8, sB, out_dtype=torch.bfloat16, bscale=BSCALE_BLOCK128, stream=None,

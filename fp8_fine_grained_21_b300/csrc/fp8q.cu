@@ -262,6 +262,34 @@ int fp8q_quant_w_128x128(const void* w, int in_dtype, int64_t N, int64_t K, uint
     return launched();
 }
 
+int fp8q_retile_1x128_to_128x1(const uint8_t* q, const float* s, int64_t T, int64_t C,
+                               uint8_t* qT, float* sT, fp8q_stream_t stream) {
+    if (!q || !s || !qT || !sT) return FP8Q_ERR_INVALID_ARG;
+    if (T <= 0 || C <= 0) return FP8Q_ERR_INVALID_ARG;
+    if (T % 128 || C % 128) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (T / 128 > 65535 || C / 64 > 0x7fffffff) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(q, 16) || !aligned(qT, 16) || !aligned(s, 4) || !aligned(sT, 4))
+        return FP8Q_ERR_MISALIGNED;
+    const dim3 grid(static_cast<unsigned>(C / 64), static_cast<unsigned>(T / 128));
+    k_retile_1x128_to_128x1<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q, s, T, C,
+                                                                                       qT, sT);
+    return launched();
+}
+
+int fp8q_transpose_w_128x128(const uint8_t* q, const float* s, int64_t N, int64_t K, uint8_t* qT,
+                             float* sT, fp8q_stream_t stream) {
+    if (!q || !s || !qT || !sT) return FP8Q_ERR_INVALID_ARG;
+    if (N <= 0 || K <= 0) return FP8Q_ERR_INVALID_ARG;
+    if (N % 128 || K % 128) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (N / 128 > 65535 || K / 128 > 0x7fffffff) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(q, 16) || !aligned(qT, 16) || !aligned(s, 4) || !aligned(sT, 4))
+        return FP8Q_ERR_MISALIGNED;
+    const dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
+    k_transpose_128x128<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q, s, N, K, qT,
+                                                                                  sT);
+    return launched();
+}
+
 int fp8q_gemm(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB, void* C,
               int64_t M, int64_t N, int64_t K, int out_dtype) {
     return gemm_common(A8, sA, B8, sB, C, nullptr, 1, M, N, K, out_dtype, FP8Q_BSCALE_BLOCK128,

@@ -12,6 +12,7 @@
 #include <cfloat>
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "ptx.cuh"
 
@@ -217,6 +218,101 @@ __global__ void __launch_bounds__(256) k_quant_128x1(const T* __restrict__ x, in
     uint4* dst = reinterpret_cast<uint4*>(qT + (c0 + c) * Tn + t0 + tp * 32);
     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// ------------------------------------------------ 1x128 tiles -> 128x1 tiles
+// Backward regrouping of the stored forward activations ("Six Reasons...",
+// para. 3): q[T][C] with 1x128 scales s[C/128][T] is dequantized -- the E4M3
+// decode is exact, times the tile scale in one correctly rounded FP32
+// multiplication -- and quantized again per 128 tokens of one channel,
+// written transposed (qT[C][T], sT[T/128][C]) like k_quant_128x1.
+// Grid (C/64, T/128), 256 threads; a 128-token x 64-channel tile of bytes and
+// the 128 token scales of its channel group are staged in shared memory.
+__device__ __forceinline__ float e4m3_to_f32(uint8_t b) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(b), __NV_E4M3);
+    return __half2float(__half(h));
+}
+
+__global__ void __launch_bounds__(256) k_retile_1x128_to_128x1(const uint8_t* __restrict__ q,
+                                                               const float* __restrict__ s,
+                                                               int64_t Tn, int64_t C,
+                                                               uint8_t* __restrict__ qT,
+                                                               float* __restrict__ sT) {
+    __shared__ __align__(16) uint8_t tile[128][64];
+    __shared__ float tscale[128];
+    __shared__ float red[4][64];
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 64;
+    const int64_t tb = blockIdx.y, t0 = tb * 128;
+    const int64_t g = c0 / 128;                       // 1x128 scale group of these channels
+#pragma unroll
+    for (int id = threadIdx.x; id < 128 * 4; id += 256) {
+        const int row = id >> 2, cc = id & 3;
+        reinterpret_cast<uint4*>(&tile[row][0])[cc] =
+            __ldcs(reinterpret_cast<const uint4*>(q + (t0 + row) * C + c0) + cc);
+    }
+    if (threadIdx.x < 128) tscale[threadIdx.x] = s[g * Tn + t0 + threadIdx.x];
+    __syncthreads();
+    const int c = threadIdx.x & 63, tp = threadIdx.x >> 6;
+    float v[32];
+    float a = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int t = tp * 32 + j;
+        v[j] = __fmul_rn(e4m3_to_f32(tile[t][c]), tscale[t]);
+        a = fmaxf(a, fabsf(v[j]));
+    }
+    red[tp][c] = a;
+    __syncthreads();
+    a = fmaxf(fmaxf(red[0][c], red[1][c]), fmaxf(red[2][c], red[3][c]));
+    float sc, inv;
+    group_scale(a, sc, inv);
+    if (tp == 0) sT[tb * C + c0 + c] = sc;
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t lo = cvt_e4m3x2(__fmul_rn(v[4 * i], inv), __fmul_rn(v[4 * i + 1], inv));
+        const uint32_t hi = cvt_e4m3x2(__fmul_rn(v[4 * i + 2], inv), __fmul_rn(v[4 * i + 3], inv));
+        w[i] = lo | (hi << 16);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(qT + (c0 + c) * Tn + t0 + tp * 32);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// ------------------------------------------------- FP8 weight transpose
+// q[N][K] (128x128 block scales s[N/128][K/128]) -> qT[K][N] with
+// sT[K/128][N/128]: the transposed weight of the data-gradient GEMM
+// dX = dY W, whose blocks and scales are the forward weight's, transposed.
+// Grid (K/128, N/128), 256 threads, one 128 x 128 byte block per CTA.
+__global__ void __launch_bounds__(256) k_transpose_128x128(const uint8_t* __restrict__ q,
+                                                           const float* __restrict__ s, int64_t N,
+                                                           int64_t K, uint8_t* __restrict__ qT,
+                                                           float* __restrict__ sT) {
+    __shared__ __align__(16) uint8_t tile[128][128 + 16];
+    const int64_t kb = blockIdx.x, nb = blockIdx.y;
+#pragma unroll
+    for (int id = threadIdx.x; id < 128 * 8; id += 256) {
+        const int row = id >> 3, cc = id & 7;
+        *reinterpret_cast<uint4*>(&tile[row][cc * 16]) =
+            __ldcs(reinterpret_cast<const uint4*>(q + (nb * 128 + row) * K + kb * 128) + cc);
+    }
+    if (threadIdx.x == 0) sT[kb * (N / 128) + nb] = s[nb * (K / 128) + kb];
+    __syncthreads();
+    // output row k (a column of the block) gets 16 consecutive n per task;
+    // a warp's lanes take 32 consecutive k of the same n range
+#pragma unroll
+    for (int id = threadIdx.x; id < 128 * 8; id += 256) {
+        const int k = id & 127, n0 = (id >> 7) * 16;
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[i] = static_cast<uint32_t>(tile[n0 + 4 * i][k]) |
+                   (static_cast<uint32_t>(tile[n0 + 4 * i + 1][k]) << 8) |
+                   (static_cast<uint32_t>(tile[n0 + 4 * i + 2][k]) << 16) |
+                   (static_cast<uint32_t>(tile[n0 + 4 * i + 3][k]) << 24);
+        *reinterpret_cast<uint4*>(qT + (kb * 128 + k) * N + nb * 128 + n0) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+    }
 }
 
 }  // namespace fp8q

@@ -17,6 +17,7 @@ Workloads (DeepSeek-V3-shaped, per the fine-grained FP8 GEMM description):
   grouped   32 experts, token counts ~ Multinomial(16384, p_i ~ i^-1.1) rounded
             up to multiples of 128; A[sum M_e][7168] BF16 N(0,1) with 0.1% x100;
             W[32][2048][7168] BF16 N(0, 0.02)
+  backward  the forward workload's A and W plus dY[4096][2048] BF16 N(0,1), 0.1% x100
 Outliers: floor(0.1% of the entries) positions drawn uniformly without
 replacement; the value already there is multiplied by the factor.
 """
@@ -25,7 +26,7 @@ import torch
 
 GROUP = 128
 
-CONFIG_NAMES = ("tiny", "forward", "accum", "wgrad", "grouped")
+CONFIG_NAMES = ("tiny", "forward", "accum", "wgrad", "grouped", "backward")
 
 
 def rng_for(seed: int, tensor_index: int) -> np.random.Generator:
@@ -109,6 +110,15 @@ def make(name: str, seed: int = 0, variant: str = "", scale_down: int = 1):
             "dY": gaussian((8192 // d, 7168 // d), rng_for(seed, 0), 1.0, 0.001, 100.0),
             "X": gaussian((8192 // d, 2048 // d), rng_for(seed, 1), 1.0, 0.001, 100.0),
             "out": "f32",
+        }
+    if name == "backward":
+        # the backward data path of the forward workload: its A and W (same
+        # streams as "forward") plus an output gradient dY[M][N]
+        return {
+            "A": gaussian((4096 // d, 7168), rng_for(seed, 0), 1.0, 0.001, 100.0),
+            "W": gaussian((2048 // d, 7168), rng_for(seed, 1), 0.02),
+            "dY": gaussian((4096 // d, 2048 // d), rng_for(seed, 2), 1.0, 0.001, 100.0),
+            "out": "bf16",
         }
     if name == "grouped":
         sizes = zipf_group_sizes(rng_for(seed, 2), tokens=16384 // d)

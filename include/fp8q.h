@@ -103,6 +103,26 @@ FP8Q_API int fp8q_quant_act_128x1(const void* x, int in_dtype, int64_t T, int64_
 FP8Q_API int fp8q_quant_w_128x128(const void* w, int in_dtype, int64_t N, int64_t K,
                          uint8_t* q, float* s, fp8q_stream_t stream);
 
+/* Backward regrouping of stored activations: "Six Reasons...", para. 3
+ * (activations converted from 1x128 tiles to 128x1 tiles in the backward
+ * pass), starting from the forward pass's stored 1x128 FP8 tiles.  Each element
+ * is dequantized (exact E4M3 decode times its tile scale, one FP32 rounding)
+ * and quantized again per 128 tokens of one channel, written transposed:
+ *   q   [T][C]  uint8 E4M3 (from fp8q_quant_act_1x128), 16-byte aligned
+ *   s   [C/128][T] float32
+ *   qT  [C][T]  uint8 E4M3, 16-byte aligned; sT [T/128][C] float32
+ * (the layout fp8q_quant_act_128x1 writes).  Requires T and C multiples of 128. */
+FP8Q_API int fp8q_retile_1x128_to_128x1(const uint8_t* q, const float* s, int64_t T, int64_t C,
+                               uint8_t* qT, float* sT, fp8q_stream_t stream);
+
+/* Transposed FP8 weight for the data-gradient GEMM dX = dY W: q[N][K] with
+ * 128x128 block scales s[N/128][K/128] -> qT[K][N] with sT[K/128][N/128]
+ * (byte-exact; the blocks and their scales are the forward weight's).  Then
+ * fp8q_gemm_ex(dY8, sdY, qT, sT, dX, T, K, N, ...) computes dX[T][K].
+ * q, qT 16-byte aligned; requires N and K multiples of 128. */
+FP8Q_API int fp8q_transpose_w_128x128(const uint8_t* q, const float* s, int64_t N, int64_t K,
+                             uint8_t* qT, float* sT, fp8q_stream_t stream);
+
 /* -------------------------------------------------------------------- GEMM */
 
 /* Block-scaled FP8 GEMM  C[M][N] = sum_k (A8[m][k] sA) (B8[n][k] sB), i.e.
