@@ -142,6 +142,22 @@ def describe(name):
     }[name]
 
 
+# ------------------------------------------------------- replicas on N ranks
+def max_over_ranks(x, dist, device):
+    """The slowest rank's time (every rank runs its own replica; the job ends
+    when the last one does)."""
+    if dist is None:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flops_per_replica, ms):
+    """Whole-job throughput: the work of all replicas over the slowest rank's time."""
+    return world * flops_per_replica / (ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- workloads
 class Workload:
     """Device buffers and the step of one workload (all kernels are fp8q's)."""
@@ -463,16 +479,9 @@ def run_fp8q(args):
     if status != 0:
         raise RuntimeError("device status after timing: %s" % fq.fp8q_status_string(status))
 
-    if dist:
-        t = torch.tensor([step_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms, dist, device)
     e2e = time_e2e(wl, max(3, min(args.steps, 20)), stream) if not args.no_e2e else None
-    e2e_ms = e2e["ms"] if e2e else None
-    if dist and e2e:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e["ms"], dist, device) if e2e else None
     if rank != 0:
         if dist:
             dist.barrier()
@@ -483,7 +492,7 @@ def run_fp8q(args):
     fp8_peak = 2.0 * peaks["bf16_tflops"]          # FP8 dense = 2 x BF16 dense (nominal ratio)
     gemm_ms = kt[2][0]
     gemm_tflops = wl.flops / (gemm_ms * 1e-3) / 1e12
-    value = world * wl.flops / (step_ms * 1e-3) / 1e12
+    value = job_tflops(world, wl.flops, step_ms)
     q_gbs = [wl.quant_bytes[i] / (kt[i][0] * 1e-3) / 1e9 for i in range(2)]
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
@@ -512,7 +521,7 @@ def run_fp8q(args):
         "wall_ms_timed_region": wall_ms,
     }
     if e2e:
-        out["e2e"] = {"value": world * wl.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+        out["e2e"] = {"value": job_tflops(world, wl.flops, e2e_ms), "unit": "TFLOPS",
                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                       "ms_per_step": e2e_ms}
     if world == 1 and not args.no_cpu_baseline:
