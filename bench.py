@@ -12,8 +12,8 @@ Prints ONE JSON line (rank 0).  `value` is whole-step throughput in TFLOPS
 resident in HBM), summed over ranks (each rank runs its own replica: weak
 scaling, no collective on the data path).  Each step is one replay of a CUDA
 graph holding the step's three kernels, timed with CUDA events on the
-launching stream; L2 is flushed (256 MB write) between timed steps, outside
-the timed events.
+launching stream; L2 is flushed between timed steps, outside the timed events
+(a 256 MB write, then a 256 MB read, so the step starts on a clean L2).
 
 --impl reference times the CPU oracle (test infrastructure, plain C) on a
 bounded sample of the same workload on this host's cores.
@@ -296,12 +296,28 @@ def capture(fn):
     return g
 
 
+class L2Flush:
+    """Evicts the step's data from L2 between timed steps: a write of a buffer
+    twice the size of L2, then a read of another one.  The read makes the
+    flush's own dirty lines drain to HBM here, outside the timed events, so
+    the next step starts with a clean L2 holding none of its inputs instead
+    of paying for the flush's write-backs."""
+
+    def __init__(self, device):
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
 def time_graph(g, n, stream, flush):
     """Mean device time of n replays, each preceded by an L2 flush that is
     outside the events (and long enough to hide the host's enqueue time)."""
     evs = []
     for _ in range(n):
-        flush.zero_()
+        flush()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -451,12 +467,12 @@ def run_fp8q(args):
     fq.load()
     wl = Workload(args.workload, seed=rank, device=device)
     stream = torch.cuda.current_stream(device)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
 
     g_step = capture(wl.step)
     g_parts = [capture(wl.quant0), capture(wl.quant1), capture(wl.gemm)]
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         g_step.replay()
     torch.cuda.synchronize()
 
@@ -501,7 +517,8 @@ def run_fp8q(args):
         "data": "synthetic (seeded PCG64; N(0,1) activations with 0.1% x100 outliers, "
                 "N(0,0.02) weights)",
         "config": {"workload": wl.desc, "M": wl.M, "N": wl.N, "K": wl.K,
-                   "l2": "flushed between timed steps (256 MB write outside the timed events)",
+                   "l2": "flushed between timed steps (256 MB write, then a 256 MB read so that "
+                         "L2 is left clean; outside the timed events)",
                    "timing": "CUDA graph replay per step, CUDA events on the launching stream",
                    "parallelism": "replicas x%d" % world},
         "gemm_tflops": gemm_tflops,

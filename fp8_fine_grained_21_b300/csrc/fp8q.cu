@@ -50,12 +50,16 @@ struct DeviceState {
     int num_sms = 0;
     int* status = nullptr;            // device address of g_status on this device
     bool gemm_attr[2][2][2] = {};     // dynamic-smem attribute set, per kernel instance
+    bool quant_attr[2][2] = {};       // the same for the staged quantizers [kind][bf16 input]
     uint8_t* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch
 };
 
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// TMA coordinates are 32-bit signed: row and column counts stay below 2^31.
+constexpr int64_t kMaxTmaCoord = 0x7fffffff;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -108,6 +112,63 @@ int encode_kmajor(CUtensorMap* map, const uint8_t* base, int64_t K, int64_t rows
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
+
+// 2-D tensor [rows][cols] of FP32 or BF16 elements, row-major, boxes of
+// box_cols x box_rows copied unswizzled (a box lands in shared memory as
+// box_rows rows of box_cols elements); rows past the end read as zeros.
+int encode_rows(CUtensorMap* map, const void* base, int in_dtype, int64_t cols, int64_t rows,
+                int box_cols, int box_rows) {
+    const bool bf = in_dtype == FP8Q_BF16;
+    const cuuint64_t es = bf ? 2 : 4;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * es};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = g_encode(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                                2, const_cast<void*>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+// Persistent quantizer launch: Cfg::kCtasPerSm CTAs per SM (fewer if there
+// are fewer tiles), each walking tiles blockIdx.x, +gridDim.x, ...
+template <typename Cfg, typename Kern>
+int launch_quant(DeviceState* d, bool& attr, Kern kern, const CUtensorMap& tm, int64_t tiles,
+                 int64_t a, int64_t b, uint8_t* q, float* s, cudaStream_t st) {
+    constexpr int kSmem = Cfg::Ring::kSmemBytes;
+    if (!attr) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+            cudaSuccess)
+            return cuda_fail();
+        attr = true;
+    }
+    int64_t grid = static_cast<int64_t>(d->num_sms) * Cfg::kCtasPerSm;
+    if (grid > tiles) grid = tiles;
+    kern<<<static_cast<unsigned>(grid), Cfg::kThreads, kSmem, st>>>(tm, a, b, q, s, d->status);
+    return cudaGetLastError() == cudaSuccess ? FP8Q_OK : cuda_fail();
+}
+
+// Input of a quantizer: BF16 or FP32, tiles of box_cols x box_rows elements.
+template <template <typename> class Cfg, template <typename> class Kern>
+int quant_common(int kind, const void* x, int in_dtype, int64_t rows, int64_t cols, int box_cols,
+                 int box_rows, int64_t tiles, uint8_t* q, float* s, fp8q_stream_t stream) {
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != FP8Q_OK) return rc;
+    CUtensorMap tm;
+    rc = encode_rows(&tm, x, in_dtype, cols, rows, box_cols, box_rows);
+    if (rc != FP8Q_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (in_dtype == FP8Q_BF16)
+        return launch_quant<Cfg<__nv_bfloat16>>(d, d->quant_attr[kind][1], Kern<__nv_bfloat16>::fn,
+                                               tm, tiles, rows, cols, q, s, st);
+    return launch_quant<Cfg<float>>(d, d->quant_attr[kind][0], Kern<float>::fn, tm, tiles, rows,
+                                    cols, q, s, st);
+}
+
+template <typename T> struct KQt { static constexpr auto fn = k_quant_128x1<T>; };
+template <typename T> struct KQw { static constexpr auto fn = k_quant_128x128<T>; };
 
 template <int BN, bool kRowB, bool kBf16>
 int launch_gemm_inst(DeviceState* d, const CUtensorMap& ta, const CUtensorMap& tb,
@@ -233,16 +294,10 @@ int fp8q_quant_act_128x1(const void* x, int in_dtype, int64_t T, int64_t C, uint
     if (!x || !qT || !sT) return FP8Q_ERR_INVALID_ARG;
     if (check_in_dtype(in_dtype) != FP8Q_OK || T <= 0 || C <= 0) return FP8Q_ERR_INVALID_ARG;
     if (T % 128 || C % 64) return FP8Q_ERR_UNSUPPORTED_SHAPE;
-    if (T / 128 > 65535 || C / 64 > 0x7fffffff) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (T > kMaxTmaCoord || C > kMaxTmaCoord) return FP8Q_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(x, 16) || !aligned(qT, 16) || !aligned(sT, 4)) return FP8Q_ERR_MISALIGNED;
-    const dim3 grid(static_cast<unsigned>(C / 64), static_cast<unsigned>(T / 128));
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (in_dtype == FP8Q_BF16)
-        k_quant_128x1<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), T,
-                                                           C, qT, sT);
-    else
-        k_quant_128x1<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), T, C, qT, sT);
-    return launched();
+    const int64_t tiles = (C / 64) * (T / 128);
+    return quant_common<QtCfg, KQt>(0, x, in_dtype, T, C, 64, 128, tiles, qT, sT, stream);
 }
 
 int fp8q_quant_w_128x128(const void* w, int in_dtype, int64_t N, int64_t K, uint8_t* q, float* s,
@@ -250,16 +305,10 @@ int fp8q_quant_w_128x128(const void* w, int in_dtype, int64_t N, int64_t K, uint
     if (!w || !q || !s) return FP8Q_ERR_INVALID_ARG;
     if (check_in_dtype(in_dtype) != FP8Q_OK || N <= 0 || K <= 0) return FP8Q_ERR_INVALID_ARG;
     if (N % 128 || K % 128) return FP8Q_ERR_UNSUPPORTED_SHAPE;
-    if (N / 128 > 65535 || K / 128 > 0x7fffffff) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (N > kMaxTmaCoord || K > kMaxTmaCoord) return FP8Q_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(w, 16) || !aligned(q, 16) || !aligned(s, 4)) return FP8Q_ERR_MISALIGNED;
-    const dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (in_dtype == FP8Q_BF16)
-        k_quant_128x128<__nv_bfloat16><<<grid, kQwThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(w), N,
-                                                             K, q, s);
-    else
-        k_quant_128x128<float><<<grid, kQwThreads, 0, st>>>(static_cast<const float*>(w), N, K, q, s);
-    return launched();
+    const int64_t tiles = (K / 128) * (N / 128);
+    return quant_common<QwCfg, KQw>(1, w, in_dtype, N, K, 128, 128, tiles, q, s, stream);
 }
 
 int fp8q_retile_1x128_to_128x1(const uint8_t* q, const float* s, int64_t T, int64_t C,

@@ -76,26 +76,95 @@ __device__ __forceinline__ uint2 quant8(const float (&v)[8], float inv) {
     return r;
 }
 
+// ------------------------------------------------------- streaming skeleton
+// The three quantizers share one structure.  A persistent grid (a few CTAs
+// per SM) walks its tiles blockIdx.x, +gridDim.x, ...  Thread 0 keeps up to
+// kStages tiles in flight, each brought into a shared-memory stage by one TMA
+// tensor copy that completes the stage's mbarrier.  Every thread copies its
+// part of the tile into registers; one CTA barrier (which also publishes
+// partial maxima and agrees on success) then frees the stage, which thread 0
+// refills with the tile kStages further on while the current tile is reduced,
+// cast and stored from registers.  HBM reads thus stay in flight across tile
+// boundaries, with no per-tile launch or ramp.
+template <int kStages, int kTileBytes>
+struct TileRing {
+    static constexpr int kBarOffset = kStages * kTileBytes;
+    static constexpr int kSmemBytes = kBarOffset + kStages * 8 + 1024;   // + alignment slack
+
+    uint8_t* base;
+    uint64_t* full;
+
+    __device__ void init(uint8_t* smem_raw) {
+        base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+        full = reinterpret_cast<uint64_t*>(base + kBarOffset);
+        if (threadIdx.x == 0) {
+#pragma unroll 1
+            for (int i = 0; i < kStages; ++i) mbar_init(&full[i], 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+    }
+    __device__ const uint8_t* stage(int i) const { return base + i * kTileBytes; }
+    __device__ void load(int i, const CUtensorMap* tm, int32_t x, int32_t y) {
+        mbar_arrive_expect_tx(&full[i], kTileBytes);
+        tma_load_2d(base + i * kTileBytes, tm, &full[i], x, y);
+    }
+    // After a failed wait: let the copies this CTA still has in flight land
+    // (n_left = tiles issued but not consumed, starting at iteration it).
+    __device__ void drain(int it, int n_left) {
+#pragma unroll 1
+        for (int j = 0; j < n_left; ++j) {
+            const int k = it + j;
+            mbar_drain(&full[k % kStages], (k / kStages) & 1, 10000000ull);
+        }
+    }
+};
+
+// Eight consecutive elements of a shared-memory tile -> FP32.
+__device__ __forceinline__ void lds8(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ void lds8(const float* p, float (&v)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0];
+    const float4 b = reinterpret_cast<const float4*>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// Tiles this CTA walks, and how many of them from iteration `it` on are
+// already in flight.
+__device__ __forceinline__ int my_tiles(int64_t tiles) {
+    return tiles > blockIdx.x ? static_cast<int>((tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+}
+
 // ------------------------------------------------------------------ 1x128
-// Grid (K/128, ceil(M / (16 * kRows))), 256 threads.  A half-warp (16 lanes
-// x 8 elements) covers one 1x128 tile; each thread handles kRows rows 16
-// apart, issuing all kRows loads before reducing.  Scales land at s[g*M + m].
-#ifndef FP8Q_Q1_ROWS
-#define FP8Q_Q1_ROWS 4
-#endif
-#ifndef FP8Q_Q1_MINB
-#define FP8Q_Q1_MINB 6
-#endif
-constexpr int kQ1RowsPerThread = FP8Q_Q1_ROWS;
+// Grid (K/128, ceil(M / 64)), 256 threads, plain 16-byte loads straight into
+// registers (at this grain, many short CTAs keep more loads in flight than a
+// staged pipeline does).  A half-warp (16 lanes x 8 elements) covers one
+// 1x128 tile; each thread handles kQ1RowsPerThread rows 16 apart, issuing all
+// its loads before reducing.  The warp's 2 * kQ1RowsPerThread tile maxima are
+// then gathered onto its first lanes, so one pass of the two correctly
+// rounded divisions serves all of them, and the results are shuffled back.
+// Scales land at s[g*M + m].
+constexpr int kQ1RowsPerThread = 4;
 constexpr int kQ1Rows = 16 * kQ1RowsPerThread;
 
 template <typename T>
-__global__ void __launch_bounds__(256, FP8Q_Q1_MINB) k_quant_1x128(const T* __restrict__ x, int64_t M,
-                                                                  int64_t K, uint8_t* __restrict__ q,
-                                                                  float* __restrict__ s) {
+__global__ void __launch_bounds__(256, 4) k_quant_1x128(const T* __restrict__ x, int64_t M,
+                                                        int64_t K, uint8_t* __restrict__ q,
+                                                        float* __restrict__ s) {
     constexpr int R = kQ1RowsPerThread;
     const int64_t g = blockIdx.x;
     const int team = threadIdx.x >> 4, tl = threadIdx.x & 15;
+    const int lane = threadIdx.x & 31, hw = lane >> 4;
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kQ1Rows + team;
     const int64_t col = g * 128 + tl * 8;
     float v[R][8];
@@ -109,6 +178,8 @@ __global__ void __launch_bounds__(256, FP8Q_Q1_MINB) k_quant_1x128(const T* __re
             for (int j = 0; j < 8; ++j) v[i][j] = 0.0f;
         }
     }
+    // tile maxima: row i of half-warp h ends up on lane 2i + h
+    float mine = 0.0f;
 #pragma unroll
     for (int i = 0; i < R; ++i) {
         float a = amax8(v[i]);
@@ -116,8 +187,15 @@ __global__ void __launch_bounds__(256, FP8Q_Q1_MINB) k_quant_1x128(const T* __re
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-        float sc, inv;
-        group_scale(a, sc, inv);
+        const float t = __shfl_sync(0xffffffffu, a, (lane & 1) << 4);
+        if ((lane >> 1) == i) mine = t;
+    }
+    float sc_l, inv_l;
+    group_scale(mine, sc_l, inv_l);
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const float inv = __shfl_sync(0xffffffffu, inv_l, 2 * i + hw);
+        const float sc = __shfl_sync(0xffffffffu, sc_l, 2 * i + hw);
         const int64_t r = r0 + 16 * i;
         if (r < M) {
             *reinterpret_cast<uint2*>(q + r * K + col) = quant8(v[i], inv);
@@ -127,97 +205,160 @@ __global__ void __launch_bounds__(256, FP8Q_Q1_MINB) k_quant_1x128(const T* __re
 }
 
 // ---------------------------------------------------------------- 128x128
-// Grid (K/128, N/128), kQwThreads threads, one block per CTA.  Thread (rr, tl)
-// holds rows rr + (kQwThreads/16) i of the block, 8 columns each, in
-// registers from the load to the store; block amax via warp shuffles and a
-// shared-memory step.
-#ifndef FP8Q_QW_THREADS
-#define FP8Q_QW_THREADS 256
-#endif
-#ifndef FP8Q_QW_MINB
-#define FP8Q_QW_MINB 1
-#endif
-constexpr int kQwThreads = FP8Q_QW_THREADS;
+// Tile = one 128x128 block of w[N][K]; thread (rr, tl) holds rows rr + 16 i
+// (i < 8), 8 columns each; block amax via warp shuffles and one shared-memory
+// step (double-buffered by iteration parity, so one CTA barrier per tile).
+template <typename T>
+struct QwCfg {
+    static constexpr int kThreads = 256;
+    static constexpr int kTileBytes = 128 * 128 * static_cast<int>(sizeof(T));
+    static constexpr int kStages = sizeof(T) == 2 ? 3 : 2;
+    static constexpr int kCtasPerSm = sizeof(T) == 2 ? 2 : 1;
+    using Ring = TileRing<kStages, kTileBytes>;
+};
 
 template <typename T>
-__global__ void __launch_bounds__(kQwThreads, FP8Q_QW_MINB) k_quant_128x128(const T* __restrict__ w,
-                                                                           int64_t N, int64_t K,
-                                                                           uint8_t* __restrict__ q,
-                                                                           float* __restrict__ s) {
-    constexpr int kWarps = kQwThreads / 32, kStride = kQwThreads / 16, R = 128 / kStride;
-    __shared__ float red[kWarps];
-    const int64_t g = blockIdx.x, nb = blockIdx.y;
-    const int64_t Kb = gridDim.x;
-    const int tl = threadIdx.x & 15, rr = threadIdx.x >> 4;
-    const int64_t col = g * 128 + tl * 8;
-    float v[R][8];
+__global__ void __launch_bounds__(256, QwCfg<T>::kCtasPerSm)
+    k_quant_128x128(const __grid_constant__ CUtensorMap tm, int64_t N, int64_t K,
+                    uint8_t* __restrict__ q, float* __restrict__ s, int* status) {
+    using C = QwCfg<T>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ float red[2][8];
+    typename C::Ring ring;
+    ring.init(smem_raw);
+    const int64_t Kb = K / 128;
+    const int64_t tiles = Kb * (N / 128);
+    const int n = my_tiles(tiles);
+    const int rr = threadIdx.x >> 4, tl = threadIdx.x & 15, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+#pragma unroll 1
+        for (int j = 0; j < C::kStages && j < n; ++j) {
+            const int64_t t = blockIdx.x + static_cast<int64_t>(j) * gridDim.x;
+            ring.load(j, &tm, static_cast<int32_t>((t % Kb) * 128), static_cast<int32_t>((t / Kb) * 128));
+        }
+    }
+#pragma unroll 1
+    for (int it = 0; it < n; ++it) {
+        const int st = it % C::kStages;
+        const int64_t t = blockIdx.x + static_cast<int64_t>(it) * gridDim.x;
+        const int64_t g = t % Kb, nb = t / Kb;
+        float v[8][8];
+        const bool got = mbar_wait(&ring.full[st], (it / C::kStages) & 1, status);
+        if (got) {
+            const T* tile = reinterpret_cast<const T*>(ring.stage(st));
+            float a = 0.0f;
 #pragma unroll
-    for (int i = 0; i < R; ++i) load8(w + (nb * 128 + rr + kStride * i) * K + col, v[i]);
-    float a = 0.0f;
+            for (int i = 0; i < 8; ++i) {
+                lds8(tile + (rr + 16 * i) * 128 + tl * 8, v[i]);
+                a = fmaxf(a, amax8(v[i]));
+            }
 #pragma unroll
-    for (int i = 0; i < R; ++i) a = fmaxf(a, amax8(v[i]));
+            for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            if ((threadIdx.x & 31) == 0) red[it & 1][warp] = a;
+        }
+        if (!__syncthreads_and(got)) {
+            if (threadIdx.x == 0) ring.drain(it, min(n - it, C::kStages));
+            return;
+        }
+        if (threadIdx.x == 0 && it + C::kStages < n) {
+            const int64_t tn = t + static_cast<int64_t>(C::kStages) * gridDim.x;
+            fence_proxy_async_smem();
+            ring.load(st, &tm, static_cast<int32_t>((tn % Kb) * 128), static_cast<int32_t>((tn / Kb) * 128));
+        }
+        float a = red[it & 1][0];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
-    __syncthreads();
-    a = red[0];
+        for (int i = 1; i < 8; ++i) a = fmaxf(a, red[it & 1][i]);
+        float sc, inv;
+        group_scale(a, sc, inv);
+        if (threadIdx.x == 0) s[nb * Kb + g] = sc;
 #pragma unroll
-    for (int i = 1; i < kWarps; ++i) a = fmaxf(a, red[i]);
-    float sc, inv;
-    group_scale(a, sc, inv);
-    if (threadIdx.x == 0) s[nb * Kb + g] = sc;
-#pragma unroll
-    for (int i = 0; i < R; ++i)
-        *reinterpret_cast<uint2*>(q + (nb * 128 + rr + kStride * i) * K + col) = quant8(v[i], inv);
+        for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<uint2*>(q + (nb * 128 + rr + 16 * i) * K + g * 128 + tl * 8) =
+                quant8(v[i], inv);
+    }
 }
 
 // ------------------------------------------------------------------ 128x1
-// Grid (C/64, T/128), 256 threads.  A 128-token x 64-channel tile is staged
-// in shared memory with coalesced 16-byte loads; thread (c, tp) then reads
-// 32 tokens of channel c (conflict-free: a warp spans 32 consecutive
-// channels), the four partial maxima of a channel meet in shared memory, and
-// the thread writes its 32 bytes of qT[c][t0 + 32 tp ..] (two 16-byte stores).
+// Tile = 128 tokens x 64 channels of x[T][C]; thread (c, tp) reads kTok
+// tokens of channel c from shared memory (conflict-free: a warp spans 32
+// consecutive channels of one token), the kParts partial maxima of a channel
+// meet in shared memory (double-buffered by iteration parity), and the
+// thread writes its kTok bytes of qT[c][t0 + kTok tp ..] (16-byte stores).
 template <typename T>
-__global__ void __launch_bounds__(256) k_quant_128x1(const T* __restrict__ x, int64_t Tn, int64_t C,
-                                                     uint8_t* __restrict__ qT,
-                                                     float* __restrict__ sT) {
-    __shared__ __align__(16) T tile[128][64];
-    __shared__ float red[4][64];
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 64;
-    const int64_t tb = blockIdx.y, t0 = tb * 128;
-    constexpr int kChunksPerRow = 64 * static_cast<int>(sizeof(T)) / 16;
-    constexpr int kChunks = 128 * kChunksPerRow;
-#pragma unroll
-    for (int id = threadIdx.x; id < kChunks; id += 256) {
-        const int row = id / kChunksPerRow, cc = id % kChunksPerRow;
-        const uint4 u = __ldcs(reinterpret_cast<const uint4*>(x + (t0 + row) * C + c0) + cc);
-        reinterpret_cast<uint4*>(&tile[row][0])[cc] = u;
-    }
-    __syncthreads();
+struct QtCfg {
+    static constexpr int kThreads = 256;
+    static constexpr int kParts = kThreads / 64;           // token ranges per channel
+    static constexpr int kTok = 128 / kParts;              // tokens per thread
+    static constexpr int kTileBytes = 128 * 64 * static_cast<int>(sizeof(T));
+    static constexpr int kStages = sizeof(T) == 2 ? 4 : 3;
+    static constexpr int kCtasPerSm = sizeof(T) == 2 ? 3 : 2;
+    using Ring = TileRing<kStages, kTileBytes>;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(QtCfg<T>::kThreads, QtCfg<T>::kCtasPerSm)
+    k_quant_128x1(const __grid_constant__ CUtensorMap tm, int64_t Tn, int64_t C,
+                  uint8_t* __restrict__ qT, float* __restrict__ sT, int* status) {
+    using Cf = QtCfg<T>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ float red[2][Cf::kParts][64];
+    typename Cf::Ring ring;
+    ring.init(smem_raw);
+    const int64_t CB = C / 64;
+    const int64_t tiles = CB * (Tn / 128);
+    const int n = my_tiles(tiles);
     const int c = threadIdx.x & 63, tp = threadIdx.x >> 6;
-    float v[32];
-    float a = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        v[j] = to_f32(tile[tp * 32 + j][c]);
-        a = fmaxf(a, fabsf(v[j]));
+    if (threadIdx.x == 0) {
+#pragma unroll 1
+        for (int j = 0; j < Cf::kStages && j < n; ++j) {
+            const int64_t t = blockIdx.x + static_cast<int64_t>(j) * gridDim.x;
+            ring.load(j, &tm, static_cast<int32_t>((t % CB) * 64), static_cast<int32_t>((t / CB) * 128));
+        }
     }
-    red[tp][c] = a;
-    __syncthreads();
-    a = fmaxf(fmaxf(red[0][c], red[1][c]), fmaxf(red[2][c], red[3][c]));
-    float sc, inv;
-    group_scale(a, sc, inv);
-    if (tp == 0) sT[tb * C + c0 + c] = sc;
-    uint32_t w[8];
+#pragma unroll 1
+    for (int it = 0; it < n; ++it) {
+        const int st = it % Cf::kStages;
+        const int64_t t = blockIdx.x + static_cast<int64_t>(it) * gridDim.x;
+        const int64_t c0 = (t % CB) * 64, tb = t / CB, t0 = tb * 128;
+        float v[Cf::kTok];
+        const bool got = mbar_wait(&ring.full[st], (it / Cf::kStages) & 1, status);
+        if (got) {
+            const T* tile = reinterpret_cast<const T*>(ring.stage(st));
+            float a = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t lo = cvt_e4m3x2(__fmul_rn(v[4 * i], inv), __fmul_rn(v[4 * i + 1], inv));
-        const uint32_t hi = cvt_e4m3x2(__fmul_rn(v[4 * i + 2], inv), __fmul_rn(v[4 * i + 3], inv));
-        w[i] = lo | (hi << 16);
+            for (int j = 0; j < Cf::kTok; ++j) {
+                v[j] = to_f32(tile[(tp * Cf::kTok + j) * 64 + c]);
+                a = fmaxf(a, fabsf(v[j]));
+            }
+            red[it & 1][tp][c] = a;
+        }
+        if (!__syncthreads_and(got)) {
+            if (threadIdx.x == 0) ring.drain(it, min(n - it, Cf::kStages));
+            return;
+        }
+        if (threadIdx.x == 0 && it + Cf::kStages < n) {
+            const int64_t tn = t + static_cast<int64_t>(Cf::kStages) * gridDim.x;
+            fence_proxy_async_smem();
+            ring.load(st, &tm, static_cast<int32_t>((tn % CB) * 64), static_cast<int32_t>((tn / CB) * 128));
+        }
+        float a = red[it & 1][0][c];
+#pragma unroll
+        for (int p = 1; p < Cf::kParts; ++p) a = fmaxf(a, red[it & 1][p][c]);
+        float sc, inv;
+        group_scale(a, sc, inv);
+        if (tp == 0) sT[tb * C + c0 + c] = sc;
+        uint32_t w[Cf::kTok / 4];
+#pragma unroll
+        for (int i = 0; i < Cf::kTok / 4; ++i) {
+            const uint32_t lo = cvt_e4m3x2(__fmul_rn(v[4 * i], inv), __fmul_rn(v[4 * i + 1], inv));
+            const uint32_t hi = cvt_e4m3x2(__fmul_rn(v[4 * i + 2], inv), __fmul_rn(v[4 * i + 3], inv));
+            w[i] = lo | (hi << 16);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(qT + (c0 + c) * Tn + t0 + tp * Cf::kTok);
+#pragma unroll
+        for (int i = 0; i < Cf::kTok / 16; ++i)
+            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
     }
-    uint4* dst = reinterpret_cast<uint4*>(qT + (c0 + c) * Tn + t0 + tp * 32);
-    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 // ------------------------------------------------ 1x128 tiles -> 128x1 tiles

@@ -90,7 +90,8 @@ FP8Q_API int fp8q_quant_act_1x128(const void* x, int in_dtype, int64_t M, int64_
  *   x   [T][C]  in_dtype, 16-byte aligned
  *   qT  [C][T]  uint8 E4M3, 16-byte aligned
  *   sT  [T/128][C] float32 (scale of channel c, token group tb at sT[tb*C + c])
- * Requires T a multiple of 128, C a multiple of 64. */
+ * Requires T a multiple of 128, C a multiple of 64, both below 2^31
+ * (FP8Q_ERR_UNSUPPORTED_SHAPE otherwise). */
 FP8Q_API int fp8q_quant_act_128x1(const void* x, int in_dtype, int64_t T, int64_t C,
                          uint8_t* qT, float* sT, fp8q_stream_t stream);
 
@@ -99,7 +100,8 @@ FP8Q_API int fp8q_quant_act_128x1(const void* x, int in_dtype, int64_t T, int64_
  *   w   [N][K]  in_dtype, 16-byte aligned
  *   q   [N][K]  uint8 E4M3, 16-byte aligned
  *   s   [N/128][K/128] float32
- * Requires N and K multiples of 128. */
+ * Requires N and K multiples of 128, both below 2^31
+ * (FP8Q_ERR_UNSUPPORTED_SHAPE otherwise). */
 FP8Q_API int fp8q_quant_w_128x128(const void* w, int in_dtype, int64_t N, int64_t K,
                          uint8_t* q, float* s, fp8q_stream_t stream);
 

@@ -178,3 +178,27 @@ def test_quant_grouped_workload(fq, oracle):
         assert_bytes_equal(qg[rows], qo, "W expert %d" % e)
         assert_scales_equal(sg[e * (N // 128) + nb:e * (N // 128) + nb + 1], so, "sW expert %d" % e)
     torch.cuda.synchronize()
+
+
+# The quantizers are persistent: a few CTAs per SM walk the tiles in turn
+# through a ring of shared-memory stages (3 or 4 deep).  These sizes give
+# every CTA more tiles than there are stages, so each stage is refilled and
+# its barrier changes phase.  Sampled rows / token blocks / block rows always
+# include the last ones, whose tiles are the last each CTA handles.
+@pytest.mark.parametrize("bf16", [True, False])
+def test_quant_1x128_many_tiles_per_cta(fq, oracle, bf16):
+    x = special_tile_input(3840 + 17, 5120, bf16, seed=91)     # 2440 tiles of 64 x 128, ragged
+    rng = np.random.default_rng(91)
+    check_1x128_rows(fq, oracle, x, _sample_rows(x.shape[0], 48, rng), "A")
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_quant_128x1_many_tiles_per_cta(fq, oracle, bf16):
+    x = special_tile_input(5120, 3840, bf16, seed=92)          # 2400 tiles of 128 x 64
+    check_128x1_tokens(fq, oracle, x, 3, np.random.default_rng(92), "x")
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_quant_128x128_many_tiles_per_cta(fq, oracle, bf16):
+    x = special_tile_input(4096, 5120, bf16, seed=93)          # 1280 blocks of 128 x 128
+    check_128x128_blocks(fq, oracle, x, 3, np.random.default_rng(93), "w")
