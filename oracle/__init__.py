@@ -45,6 +45,7 @@ def _load():
         for name in ("fpo_quant_1x128", "fpo_quant_128x1", "fpo_quant_128x128"):
             getattr(lib, name).argtypes = [P, I64, I64, P, P]
         lib.fpo_retile_1x128_to_128x1.argtypes = [P, P, I64, I64, P, P]
+        lib.fpo_swiglu_f64.argtypes = [P, P, I64, P]
         lib.fpo_gemm_f64.argtypes = [P, P, P, P, I, I64, I64, I64, P, P, I]
         lib.fpo_gemm_f64_entries.argtypes = [P, P, P, P, I, I64, I64, I64, P, P, I64, P, P, I]
         lib.fpo_gemm_grouped_f64.argtypes = [P, P, P, P, P, I64, I64, I64, I64, P, P, I]
@@ -152,6 +153,27 @@ def retile_1x128_to_128x1(q, s):
     sT = np.empty((_nb(T), C), np.float32)
     _load().fpo_retile_1x128_to_128x1(_ptr(q), _ptr(s), T, C, _ptr(qT), _ptr(sT))
     return qT, sT
+
+
+def swiglu_f64(g, u):
+    """SwiGLU(g, u) = silu(g) * u = g u / (1 + e^-g) in FP64 (the SwiGLU
+    operator of the woojincopolymer post, para. 4).  g, u: same shape, FP32 or
+    BF16 bits."""
+    g = widen(g)
+    u = widen(u)
+    assert g.shape == u.shape
+    h = np.empty(g.shape, np.float64)
+    _load().fpo_swiglu_f64(_ptr(g), _ptr(u), g.size, _ptr(h))
+    return h
+
+
+def swiglu_quant_1x128(g, u):
+    """Fused SwiGLU + 1x128 FP8 cast (woojincopolymer post, paras. 3-4): the
+    exact SwiGLU output rounded once to FP32, quantized per 1x128 tile.
+    g, u [M][I] -> (q[M][I] uint8, s[ceil(I/128)][M] float32, h[M][I] FP64)."""
+    h = swiglu_f64(g, u)
+    q, s = quant_1x128(h.astype(np.float32))
+    return q, s, h
 
 
 def dequant_1x128(q, s):

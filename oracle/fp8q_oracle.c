@@ -243,6 +243,24 @@ void fpo_retile_1x128_to_128x1(const uint8_t* q, const float* s, int64_t T, int6
     free(x);
 }
 
+/* ---------------------------------------------------- SwiGLU + FP8 cast */
+
+/* [P2] para. 4: the SwiGLU operator's inputs are cached and its output is
+ * recomputed in the backward pass; forward activations are stored as 1x128
+ * FP8 tiles.  [P2] para. 3: fusing the FP8 cast into the operator that
+ * produces the activation.  SwiGLU(g, u) = silu(g) * u with
+ * silu(g) = g * sigmoid(g) = g / (1 + e^-g).  Evaluated here in FP64 for each
+ * of the n elements of g and u (FP32, widened from BF16 by the caller); the
+ * fused quantization is fpo_quant_1x128 applied to the FP64 result rounded
+ * once to FP32 (the wrapper does that step). */
+void fpo_swiglu_f64(const float* g, const float* u, int64_t n, double* h)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        double gi = (double)g[i];
+        h[i] = gi * (double)u[i] / (1.0 + exp(-gi));
+    }
+}
+
 /* ------------------------------------------------------------------- GEMM */
 
 /* Scale of operand B for output column n and K group g.
