@@ -34,6 +34,7 @@ STATUS_NAMES = {0: "FP8Q_OK", 1: "FP8Q_ERR_INVALID_ARG", 2: "FP8Q_ERR_UNSUPPORTE
                 3: "FP8Q_ERR_MISALIGNED", 4: "FP8Q_ERR_CUDA", 5: "FP8Q_ERR_TIMEOUT",
                 6: "FP8Q_ERR_BAD_GROUPS"}
 EXPORTS = ("fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128",
+           "fp8q_swiglu_quant_1x128",
            "fp8q_retile_1x128_to_128x1", "fp8q_transpose_w_128x128", "fp8q_gemm",
            "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_gemm_ws", "fp8q_gemm_grouped_ws",
            "fp8q_gemm_workspace_size", "fp8q_gemm_noalloc", "fp8q_get_device_status",
@@ -67,6 +68,8 @@ def load():
         f = getattr(lib, name)
         f.argtypes = [P, I, I64, I64, P, P, P]
         f.restype = I
+    lib.fp8q_swiglu_quant_1x128.argtypes = [P, P, I, I64, I64, I64, P, P, P]
+    lib.fp8q_swiglu_quant_1x128.restype = I
     for name in ("fp8q_retile_1x128_to_128x1", "fp8q_transpose_w_128x128"):
         f = getattr(lib, name)
         f.argtypes = [P, P, I64, I64, P, P, P]
@@ -147,6 +150,32 @@ def fp8q_quant_act_1x128(x, q, s, stream=None):
     M, K = x.shape
     _check("fp8q_quant_act_1x128", load().fp8q_quant_act_1x128(
         _dev(x, "x"), _in_dtype(x), M, K, _dev(q, "q", torch.uint8),
+        _dev(s, "s", torch.float32), _stream(stream)))
+
+
+def _rows(t: torch.Tensor, name: str):
+    """Pointer and row stride (elements) of a 2-D CUDA tensor with unit column stride."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (no CPU path)" % name)
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("%s must be 2-D with unit column stride" % name)
+    return ctypes.c_void_p(t.data_ptr()), t.stride(0)
+
+
+def fp8q_swiglu_quant_1x128(gate, up, q, s, stream=None):
+    """gate, up: [M][I] views with the same row stride (e.g. the two halves of
+    a [M][2I] projection output)."""
+    if gate.shape != up.shape or gate.dtype != up.dtype:
+        raise ValueError("gate and up must have the same shape and dtype")
+    pg, ld = _rows(gate, "gate")
+    pu, ldu = _rows(up, "up")
+    if ldu != ld:
+        raise ValueError("gate and up must have the same row stride")
+    M, I = gate.shape
+    _check("fp8q_swiglu_quant_1x128", load().fp8q_swiglu_quant_1x128(
+        pg, pu, _in_dtype(gate), M, I, ld, _dev(q, "q", torch.uint8),
         _dev(s, "s", torch.float32), _stream(stream)))
 
 
@@ -292,6 +321,15 @@ def quant_act_1x128(x, stream=None):
     q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     s = torch.empty((_scales(K), M), dtype=torch.float32, device=x.device)
     fp8q_quant_act_1x128(x, q, s, stream)
+    return q, s
+
+
+def swiglu_quant_1x128(gate, up, stream=None):
+    """silu(gate) * up, quantized 1x128: -> (q[M][I] uint8, s[I/128][M] float32)."""
+    M, I = gate.shape
+    q = torch.empty((M, I), dtype=torch.uint8, device=gate.device)
+    s = torch.empty((_scales(I), M), dtype=torch.float32, device=gate.device)
+    fp8q_swiglu_quant_1x128(gate, up, q, s, stream)
     return q, s
 
 

@@ -289,6 +289,31 @@ int fp8q_quant_act_1x128(const void* x, int in_dtype, int64_t M, int64_t K, uint
     return launched();
 }
 
+int fp8q_swiglu_quant_1x128(const void* gate, const void* up, int in_dtype, int64_t M, int64_t I,
+                            int64_t ld, uint8_t* q, float* s, fp8q_stream_t stream) {
+    if (!gate || !up || !q || !s) return FP8Q_ERR_INVALID_ARG;
+    if (check_in_dtype(in_dtype) != FP8Q_OK || M <= 0 || I <= 0 || ld < I)
+        return FP8Q_ERR_INVALID_ARG;
+    if (I % 128) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    const int64_t yblocks = (M + kSwRows - 1) / kSwRows;
+    if (yblocks > 65535 || I / 128 > 0x7fffffff) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    const int64_t es = in_dtype == FP8Q_BF16 ? 2 : 4;
+    if (!aligned(gate, 16) || !aligned(up, 16) || (ld * es) % 16 || !aligned(q, 16) ||
+        !aligned(s, 4))
+        return FP8Q_ERR_MISALIGNED;
+    const dim3 grid(static_cast<unsigned>(I / 128), static_cast<unsigned>(yblocks));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (in_dtype == FP8Q_BF16)
+        k_swiglu_quant_1x128<__nv_bfloat16><<<grid, 256, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(gate), static_cast<const __nv_bfloat16*>(up), M, I,
+            ld, q, s);
+    else
+        k_swiglu_quant_1x128<float><<<grid, 256, 0, st>>>(static_cast<const float*>(gate),
+                                                          static_cast<const float*>(up), M, I, ld,
+                                                          q, s);
+    return launched();
+}
+
 int fp8q_quant_act_128x1(const void* x, int in_dtype, int64_t T, int64_t C, uint8_t* qT, float* sT,
                          fp8q_stream_t stream) {
     if (!x || !qT || !sT) return FP8Q_ERR_INVALID_ARG;

@@ -204,6 +204,78 @@ __global__ void __launch_bounds__(256, 4) k_quant_1x128(const T* __restrict__ x,
     }
 }
 
+// ------------------------------------------------- SwiGLU + 1x128 FP8 cast
+// The down projection's FP8 input made in one pass (woojincopolymer post,
+// para. 3: the FP8 cast fused into the operator that produces the
+// activation; para. 4: the SwiGLU output, recomputed from its cached inputs,
+// kept as 1x128 FP8 tiles).  h = silu(g) * u = g u / (1 + e^-g) in FP32, then
+// the 1x128 rule of k_quant_1x128; h never reaches memory.  Same grid, lane
+// layout and lane-parallel scales as k_quant_1x128, with kSwRowsPerThread
+// rows per thread.  Gate and up rows are ld elements apart, so ld = 2I reads
+// the two halves of one [M][2I] projection output in place.
+constexpr int kSwRowsPerThread = 4;
+constexpr int kSwRows = 16 * kSwRowsPerThread;
+
+// silu(g) * u in FP32: expf (the accurate one, a few ulp) and IEEE division.
+// For g below about -88, e^-g overflows and the result is a zero with the sign
+// of -u, as the exact value rounds to.
+__device__ __forceinline__ float swiglu_f32(float g, float u) {
+    const float e = expf(-g);
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), u);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256, 3) k_swiglu_quant_1x128(const T* __restrict__ gate,
+                                                               const T* __restrict__ up,
+                                                               int64_t M, int64_t I, int64_t ld,
+                                                               uint8_t* __restrict__ q,
+                                                               float* __restrict__ s) {
+    constexpr int R = kSwRowsPerThread;
+    const int64_t g = blockIdx.x;
+    const int team = threadIdx.x >> 4, tl = threadIdx.x & 15;
+    const int lane = threadIdx.x & 31, hw = lane >> 4;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kSwRows + team;
+    const int64_t col = g * 128 + tl * 8;
+    float v[R][8];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const int64_t r = r0 + 16 * i;
+        if (r < M) {
+            float gv[8], uv[8];
+            load8(gate + r * ld + col, gv);
+            load8(up + r * ld + col, uv);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[i][j] = swiglu_f32(gv[j], uv[j]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[i][j] = 0.0f;
+        }
+    }
+    float mine = 0.0f;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        float a = amax8(v[i]);
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        const float t = __shfl_sync(0xffffffffu, a, (lane & 1) << 4);
+        if ((lane >> 1) == i) mine = t;
+    }
+    float sc_l, inv_l;
+    group_scale(mine, sc_l, inv_l);
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const float inv = __shfl_sync(0xffffffffu, inv_l, 2 * i + hw);
+        const float sc = __shfl_sync(0xffffffffu, sc_l, 2 * i + hw);
+        const int64_t r = r0 + 16 * i;
+        if (r < M) {
+            *reinterpret_cast<uint2*>(q + r * I + col) = quant8(v[i], inv);
+            if (tl == 0) s[g * M + r] = sc;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- 128x128
 // Tile = one 128x128 block of w[N][K]; thread (rr, tl) holds rows rr + 16 i
 // (i < 8), 8 columns each; block amax via warp shuffles and one shared-memory

@@ -18,6 +18,8 @@ Workloads (DeepSeek-V3-shaped, per the fine-grained FP8 GEMM description):
             up to multiples of 128; A[sum M_e][7168] BF16 N(0,1) with 0.1% x100;
             W[32][2048][7168] BF16 N(0, 0.02)
   backward  the forward workload's A and W plus dY[4096][2048] BF16 N(0,1), 0.1% x100
+  mlp_down  gate_up[4096][2*2048] BF16 N(0,1), 0.1% x100 (gate | up halves of the
+            up-projection output); W2[7168][2048] BF16 N(0, 0.02)
 Outliers: floor(0.1% of the entries) positions drawn uniformly without
 replacement; the value already there is multiplied by the factor.
 """
@@ -26,7 +28,7 @@ import torch
 
 GROUP = 128
 
-CONFIG_NAMES = ("tiny", "forward", "accum", "wgrad", "grouped", "backward")
+CONFIG_NAMES = ("tiny", "forward", "accum", "wgrad", "grouped", "backward", "mlp_down")
 
 
 def rng_for(seed: int, tensor_index: int) -> np.random.Generator:
@@ -128,6 +130,14 @@ def make(name: str, seed: int = 0, variant: str = "", scale_down: int = 1):
             "A": gaussian((mtot, 7168), rng_for(seed, 0), 1.0, 0.001, 100.0),
             "W": gaussian((32, 2048 // d, 7168), rng_for(seed, 1), 0.02),
             "m_offsets": offs,
+            "out": "bf16",
+        }
+    if name == "mlp_down":
+        # SwiGLU MLP down projection: the gate and up halves of the up
+        # projection's output side by side, and the down-projection weight
+        return {
+            "gate_up": gaussian((4096 // d, 2 * 2048), rng_for(seed, 0), 1.0, 0.001, 100.0),
+            "W2": gaussian((7168 // d, 2048), rng_for(seed, 1), 0.02),
             "out": "bf16",
         }
     raise ValueError("unknown workload %r" % name)

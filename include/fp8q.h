@@ -83,6 +83,23 @@ typedef enum {
 FP8Q_API int fp8q_quant_act_1x128(const void* x, int in_dtype, int64_t M, int64_t K,
                          uint8_t* q, float* s, fp8q_stream_t stream);
 
+/* Fused SwiGLU + 1x128 FP8 cast: h = silu(gate) * up = gate * up / (1 + e^-gate),
+ * computed in FP32 and quantized per 1x128 tile exactly like
+ * fp8q_quant_act_1x128, without h being written.  woojincopolymer post,
+ * para. 3 (the FP8 cast fused into the operator producing the activation) and
+ * para. 4 (the SwiGLU output, recomputed from cached inputs, kept as 1x128
+ * FP8 tiles).  h carries FP32 rounding (e^-gate to a few ulp), so results
+ * match a correctly rounded evaluation to within a few FP32 ulp of h before
+ * the cast, not bit for bit.
+ *   gate, up  [M][I] in_dtype, row m at gate + m*ld and up + m*ld (ld >= I
+ *             elements; ld = 2I with up = gate + I reads one [M][2I] tensor);
+ *             16-byte aligned, ld * element size a multiple of 16
+ *   q   [M][I]  uint8 E4M3 (contiguous), 16-byte aligned
+ *   s   [I/128][M] float32, 4-byte aligned
+ * Requires M >= 1, I a multiple of 128. */
+FP8Q_API int fp8q_swiglu_quant_1x128(const void* gate, const void* up, int in_dtype, int64_t M,
+                         int64_t I, int64_t ld, uint8_t* q, float* s, fp8q_stream_t stream);
+
 /* Activations regrouped for the backward pass, one scale per 128x1 tile
  * (128 consecutive tokens of one channel), written transposed so that the
  * result is a K-major GEMM operand whose K runs over tokens:

@@ -76,6 +76,17 @@ def test_quant_argument_checks(lib):
     assert h(A16, 0, 128, 128, MIS, A16c, None) == 3
 
 
+def test_swiglu_quant_argument_checks(lib):
+    f = lib.fp8q_swiglu_quant_1x128
+    assert f(None, A16, 1, 64, 256, 512, A16b, A16c, None) == 1     # null gate
+    assert f(A16, A16, 5, 64, 256, 512, A16b, A16c, None) == 1      # bad dtype
+    assert f(A16, A16, 1, 0, 256, 512, A16b, A16c, None) == 1       # empty
+    assert f(A16, A16, 1, 64, 256, 128, A16b, A16c, None) == 1      # ld < I
+    assert f(A16, A16, 1, 64, 200, 512, A16b, A16c, None) == 2      # I not a multiple of 128
+    assert f(A16, MIS, 1, 64, 256, 512, A16b, A16c, None) == 3      # misaligned up
+    assert f(A16, A16, 1, 64, 256, 260, A16b, A16c, None) == 3      # row stride not 16-byte
+
+
 def test_gemm_argument_checks(lib):
     g = lib.fp8q_gemm_ex
     ok = (A16, A16b, A16c, P(0x40000), P(0x50000))
