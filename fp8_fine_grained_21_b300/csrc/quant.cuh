@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(256, 4) k_quant_1x128(const T* __restrict__ x,
 // layout and lane-parallel scales as k_quant_1x128, with kSwRowsPerThread
 // rows per thread.  Gate and up rows are ld elements apart, so ld = 2I reads
 // the two halves of one [M][2I] projection output in place.
-constexpr int kSwRowsPerThread = 4;
+constexpr int kSwRowsPerThread = 2;
 constexpr int kSwRows = 16 * kSwRowsPerThread;
 
 // silu(g) * u in FP32: expf (the accurate one, a few ulp) and IEEE division.
@@ -225,7 +225,7 @@ __device__ __forceinline__ float swiglu_f32(float g, float u) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256, 3) k_swiglu_quant_1x128(const T* __restrict__ gate,
+__global__ void __launch_bounds__(256, 6) k_swiglu_quant_1x128(const T* __restrict__ gate,
                                                                const T* __restrict__ up,
                                                                int64_t M, int64_t I, int64_t ld,
                                                                uint8_t* __restrict__ q,
