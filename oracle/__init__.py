@@ -46,6 +46,7 @@ def _load():
             getattr(lib, name).argtypes = [P, I64, I64, P, P]
         lib.fpo_retile_1x128_to_128x1.argtypes = [P, P, I64, I64, P, P]
         lib.fpo_swiglu_f64.argtypes = [P, P, I64, P]
+        lib.fpo_rmsnorm_f64.argtypes = [P, P, I64, I64, ctypes.c_double, P]
         lib.fpo_gemm_f64.argtypes = [P, P, P, P, I, I64, I64, I64, P, P, I]
         lib.fpo_gemm_f64_entries.argtypes = [P, P, P, P, I, I64, I64, I64, P, P, I64, P, P, I]
         lib.fpo_gemm_grouped_f64.argtypes = [P, P, P, P, P, I64, I64, I64, I64, P, P, I]
@@ -174,6 +175,27 @@ def swiglu_quant_1x128(g, u):
     h = swiglu_f64(g, u)
     q, s = quant_1x128(h.astype(np.float32))
     return q, s, h
+
+
+def rmsnorm_f64(x, w, eps):
+    """RMSNorm y = x w / sqrt(mean(x^2) + eps) per row, in FP64 (the layer
+    normalization of the woojincopolymer post, para. 3).  x[M][K], w[K]."""
+    x = widen(x)
+    w = widen(w)
+    M, K = x.shape
+    assert w.shape == (K,)
+    y = np.empty((M, K), np.float64)
+    _load().fpo_rmsnorm_f64(_ptr(x), _ptr(w), M, K, float(eps), _ptr(y))
+    return y
+
+
+def rmsnorm_quant_1x128(x, w, eps):
+    """Fused RMSNorm + 1x128 FP8 cast (woojincopolymer post, para. 3): the
+    exact normalized value rounded once to FP32, quantized per 1x128 tile.
+    -> (q[M][K] uint8, s[ceil(K/128)][M] float32, y[M][K] FP64)."""
+    y = rmsnorm_f64(x, w, eps)
+    q, s = quant_1x128(y.astype(np.float32))
+    return q, s, y
 
 
 def dequant_1x128(q, s):

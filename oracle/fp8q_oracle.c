@@ -261,6 +261,28 @@ void fpo_swiglu_f64(const float* g, const float* u, int64_t n, double* h)
     }
 }
 
+/* --------------------------------------------------- RMSNorm + FP8 cast */
+
+/* [P2] para. 3: a warp-level cast instruction is proposed so that layer
+ * normalization and the FP8 cast can be fused.  DeepSeek-V3's normalization
+ * is RMSNorm: y[m][k] = x[m][k] * w[k] / sqrt(mean_k x[m][k]^2 + eps).
+ * Evaluated here in FP64 for each row of x[M][K] (FP32, widened from BF16 by
+ * the caller), weights w[K]; the fused quantization is fpo_quant_1x128
+ * applied to the FP64 result rounded once to FP32 (the wrapper does that). */
+void fpo_rmsnorm_f64(const float* x, const float* w, int64_t M, int64_t K, double eps, double* y)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double v = (double)x[m * K + k];
+            ss += v * v;
+        }
+        double rms = sqrt(ss / (double)K + eps);
+        for (int64_t k = 0; k < K; ++k)
+            y[m * K + k] = (double)x[m * K + k] * (double)w[k] / rms;
+    }
+}
+
 /* ------------------------------------------------------------------- GEMM */
 
 /* Scale of operand B for output column n and K group g.
