@@ -38,6 +38,7 @@ import fp8q_inputs as fi  # noqa: E402
 
 METRIC = "block-scaled FP8 GEMM TFLOPS (% of FP8 peak); quantize GB/s (% of HBM)"
 FLUSH_BYTES = 256 << 20
+RMS_EPS = 1e-6                  # RMSNorm epsilon of the forward_norm workload
 
 
 # ------------------------------------------------------------------ helpers
@@ -136,6 +137,9 @@ def describe(name):
         "accum": "accum: A[1024][16384] x B[1024][16384] bf16 U(-1,1), 1x128 / 128x128 -> f32",
         "grouped": "grouped: 32 experts (Multinomial(16384, Zipf 1.1), M_e rounded up to 128), "
                    "N=2048, K=7168, bf16 -> bf16",
+        "forward_norm": "forward with fused RMSNorm: X[4096][7168] bf16 -> fused RMSNorm (g[7168], "
+                        "eps 1e-6) + 1x128 FP8 cast, x W[2048][7168] bf16 128x128-quantized -> "
+                        "C[4096][2048] bf16",
         "mlp_down": "SwiGLU MLP down projection: gate_up[4096][2*2048] bf16 -> fused "
                     "silu(gate)*up + 1x128 FP8 cast, W2[7168][2048] bf16 128x128-quantized, "
                     "C[4096][7168] = h W2^T -> bf16",
@@ -192,6 +196,11 @@ class Workload:
             self.inputs_host = [d["dY"], d["A"], d["W"]]
             self.out_dtype = torch.bfloat16
             self.launches_per_step = 4
+        elif name == "forward_norm":
+            self.M, self.K = d["X"].shape
+            self.N = d["W"].shape[0]
+            self.inputs_host = [d["X"], d["W"], d["g"]]
+            self.out_dtype = torch.bfloat16
         elif name == "mlp_down":
             gu, W2 = d["gate_up"], d["W2"]
             self.M, self.K = gu.shape[0], gu.shape[1] // 2
@@ -223,6 +232,9 @@ class Workload:
         elif name == "wgrad":
             self.a8, self.sa = fq.quant_act_128x1(x0)
             self.b8, self.sb = fq.quant_act_128x1(x1)
+        elif name == "forward_norm":
+            self.a8, self.sa = fq.rmsnorm_quant_1x128(x0, self.inputs[2], RMS_EPS)
+            self.b8, self.sb = fq.quant_w_128x128(x1)
         elif name == "mlp_down":
             self.a8, self.sa = fq.swiglu_quant_1x128(x0[:, :self.K], x0[:, self.K:])
             self.b8, self.sb = fq.quant_w_128x128(x1)
@@ -259,8 +271,13 @@ class Workload:
             fq.fp8q_quant_act_128x1(self.inputs[0], self.a8, self.sa, stream)
         elif self.name == "mlp_down":
             self._swiglu(self.inputs[0], self.a8, self.sa, stream)
+        elif self.name == "forward_norm":
+            self._rmsnorm(self.inputs[0], self.a8, self.sa, stream)
         else:
             fq.fp8q_quant_act_1x128(self.inputs[0], self.a8, self.sa, stream)
+
+    def _rmsnorm(self, x, q, s, stream):
+        self.fq.fp8q_rmsnorm_quant_1x128(x, self.inputs[2], q, s, RMS_EPS, stream)
 
     def _swiglu(self, gu, q, s, stream):
         self.fq.fp8q_swiglu_quant_1x128(gu[:, :self.K], gu[:, self.K:], q, s, stream)
@@ -296,6 +313,9 @@ class Workload:
                     (self.inputs[1], fq.fp8q_quant_act_128x1, self.b8, self.sb)]
         if self.name == "backward":
             return [(self.inputs[0], fq.fp8q_quant_act_1x128, self.a8, self.sa)]
+        if self.name == "forward_norm":
+            return [(self.inputs[0], self._rmsnorm, self.a8, self.sa),
+                    (self.inputs[1], fq.fp8q_quant_w_128x128, self.b8, self.sb)]
         if self.name == "mlp_down":
             return [(self.inputs[0], self._swiglu, self.a8, self.sa),
                     (self.inputs[1], fq.fp8q_quant_w_128x128, self.b8, self.sb)]
@@ -457,6 +477,11 @@ def oracle_sample(name, rows, kcols=None, seed=0, threads=0, data=None):
             M, K = A.shape[0], A.shape[1] // 2
             N = B.shape[0]
             full_elems = M * K + B.size
+        elif name == "forward_norm":
+            A, B = d["X"], d["W"]
+            M, K = A.shape
+            N = B.shape[0]
+            full_elems = A.size + B.size
         else:
             A, B = (d["A"], d["W"]) if name == "forward" else (d["A"], d["B"])
             M, K = A.shape
@@ -464,7 +489,10 @@ def oracle_sample(name, rows, kcols=None, seed=0, threads=0, data=None):
             full_elems = A.size + B.size
         kc = K if kcols is None else min(kcols, K)
         t0 = time.perf_counter()
-        if name == "mlp_down":
+        if name == "forward_norm":
+            a8, sa, _ = oracle.rmsnorm_quant_1x128(np.ascontiguousarray(A[:rows, :kc]),
+                                                   np.ascontiguousarray(d["g"][:kc]), RMS_EPS)
+        elif name == "mlp_down":
             a8, sa, _ = oracle.swiglu_quant_1x128(np.ascontiguousarray(A[:rows, :kc]),
                                                   np.ascontiguousarray(A[:rows, K:K + kc]))
         else:
@@ -640,7 +668,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["fp8q", "reference"], default="fp8q")
     ap.add_argument("--workload", choices=["forward", "wgrad", "accum", "grouped", "backward",
-                                           "mlp_down"],
+                                           "mlp_down", "forward_norm"],
                     default="forward")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

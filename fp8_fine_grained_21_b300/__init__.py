@@ -34,7 +34,7 @@ STATUS_NAMES = {0: "FP8Q_OK", 1: "FP8Q_ERR_INVALID_ARG", 2: "FP8Q_ERR_UNSUPPORTE
                 3: "FP8Q_ERR_MISALIGNED", 4: "FP8Q_ERR_CUDA", 5: "FP8Q_ERR_TIMEOUT",
                 6: "FP8Q_ERR_BAD_GROUPS"}
 EXPORTS = ("fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128",
-           "fp8q_swiglu_quant_1x128",
+           "fp8q_swiglu_quant_1x128", "fp8q_rmsnorm_quant_1x128",
            "fp8q_retile_1x128_to_128x1", "fp8q_transpose_w_128x128", "fp8q_gemm",
            "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_gemm_ws", "fp8q_gemm_grouped_ws",
            "fp8q_gemm_workspace_size", "fp8q_gemm_noalloc", "fp8q_get_device_status",
@@ -70,6 +70,8 @@ def load():
         f.restype = I
     lib.fp8q_swiglu_quant_1x128.argtypes = [P, P, I, I64, I64, I64, P, P, P]
     lib.fp8q_swiglu_quant_1x128.restype = I
+    lib.fp8q_rmsnorm_quant_1x128.argtypes = [P, P, I, I64, I64, ctypes.c_float, P, P, P]
+    lib.fp8q_rmsnorm_quant_1x128.restype = I
     for name in ("fp8q_retile_1x128_to_128x1", "fp8q_transpose_w_128x128"):
         f = getattr(lib, name)
         f.argtypes = [P, P, I64, I64, P, P, P]
@@ -177,6 +179,16 @@ def fp8q_swiglu_quant_1x128(gate, up, q, s, stream=None):
     _check("fp8q_swiglu_quant_1x128", load().fp8q_swiglu_quant_1x128(
         pg, pu, _in_dtype(gate), M, I, ld, _dev(q, "q", torch.uint8),
         _dev(s, "s", torch.float32), _stream(stream)))
+
+
+def fp8q_rmsnorm_quant_1x128(x, w, q, s, eps=1e-6, stream=None):
+    """x [M][K], w [K] (same dtype); eps > 0."""
+    M, K = x.shape
+    if w.dtype != x.dtype or tuple(w.shape) != (K,):
+        raise ValueError("w must be [K] with x's dtype")
+    _check("fp8q_rmsnorm_quant_1x128", load().fp8q_rmsnorm_quant_1x128(
+        _dev(x, "x"), _dev(w, "w"), _in_dtype(x), M, K, ctypes.c_float(eps),
+        _dev(q, "q", torch.uint8), _dev(s, "s", torch.float32), _stream(stream)))
 
 
 def fp8q_quant_act_128x1(x, qT, sT, stream=None):
@@ -330,6 +342,15 @@ def swiglu_quant_1x128(gate, up, stream=None):
     q = torch.empty((M, I), dtype=torch.uint8, device=gate.device)
     s = torch.empty((_scales(I), M), dtype=torch.float32, device=gate.device)
     fp8q_swiglu_quant_1x128(gate, up, q, s, stream)
+    return q, s
+
+
+def rmsnorm_quant_1x128(x, w, eps=1e-6, stream=None):
+    """RMSNorm(x) * w, quantized 1x128: -> (q[M][K] uint8, s[K/128][M] float32)."""
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    s = torch.empty((_scales(K), M), dtype=torch.float32, device=x.device)
+    fp8q_rmsnorm_quant_1x128(x, w, q, s, eps, stream)
     return q, s
 
 

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <cfloat>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -311,6 +312,26 @@ int fp8q_swiglu_quant_1x128(const void* gate, const void* up, int in_dtype, int6
         k_swiglu_quant_1x128<float><<<grid, 256, 0, st>>>(static_cast<const float*>(gate),
                                                           static_cast<const float*>(up), M, I, ld,
                                                           q, s);
+    return launched();
+}
+
+int fp8q_rmsnorm_quant_1x128(const void* x, const void* w, int in_dtype, int64_t M, int64_t K,
+                             float eps, uint8_t* q, float* s, fp8q_stream_t stream) {
+    if (!x || !w || !q || !s) return FP8Q_ERR_INVALID_ARG;
+    if (check_in_dtype(in_dtype) != FP8Q_OK || M <= 0 || K <= 0) return FP8Q_ERR_INVALID_ARG;
+    if (!(eps > 0.0f) || eps > FLT_MAX) return FP8Q_ERR_INVALID_ARG;
+    if (K % 128 || K > kRnMaxK || M > 0x7fffffff) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(q, 16) || !aligned(s, 4))
+        return FP8Q_ERR_MISALIGNED;
+    const unsigned threads = static_cast<unsigned>((K / 16 + 31) / 32 * 32);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (in_dtype == FP8Q_BF16)
+        k_rmsnorm_quant_1x128<__nv_bfloat16><<<static_cast<unsigned>(M), threads, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w), M, K, eps,
+            q, s);
+    else
+        k_rmsnorm_quant_1x128<float><<<static_cast<unsigned>(M), threads, 0, st>>>(
+            static_cast<const float*>(x), static_cast<const float*>(w), M, K, eps, q, s);
     return launched();
 }
 

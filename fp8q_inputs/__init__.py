@@ -20,6 +20,9 @@ Workloads (DeepSeek-V3-shaped, per the fine-grained FP8 GEMM description):
   backward  the forward workload's A and W plus dY[4096][2048] BF16 N(0,1), 0.1% x100
   mlp_down  gate_up[4096][2*2048] BF16 N(0,1), 0.1% x100 (gate | up halves of the
             up-projection output); W2[7168][2048] BF16 N(0, 0.02)
+  forward_norm  the forward workload with its activations normalized first:
+            X[4096][7168] BF16 N(0,1), 0.1% x100 (un-normalized), RMSNorm weight
+            g[7168] BF16 N(1, 0.1), W[2048][7168] BF16 N(0, 0.02)
 Outliers: floor(0.1% of the entries) positions drawn uniformly without
 replacement; the value already there is multiplied by the factor.
 """
@@ -28,7 +31,8 @@ import torch
 
 GROUP = 128
 
-CONFIG_NAMES = ("tiny", "forward", "accum", "wgrad", "grouped", "backward", "mlp_down")
+CONFIG_NAMES = ("tiny", "forward", "accum", "wgrad", "grouped", "backward", "mlp_down",
+                "forward_norm")
 
 
 def rng_for(seed: int, tensor_index: int) -> np.random.Generator:
@@ -130,6 +134,14 @@ def make(name: str, seed: int = 0, variant: str = "", scale_down: int = 1):
             "A": gaussian((mtot, 7168), rng_for(seed, 0), 1.0, 0.001, 100.0),
             "W": gaussian((32, 2048 // d, 7168), rng_for(seed, 1), 0.02),
             "m_offsets": offs,
+            "out": "bf16",
+        }
+    if name == "forward_norm":
+        g = (1.0 + 0.1 * rng_for(seed, 2).standard_normal(7168)).astype(np.float32)
+        return {
+            "X": gaussian((4096 // d, 7168), rng_for(seed, 0), 1.0, 0.001, 100.0),
+            "g": to_bf16_bits(g),
+            "W": gaussian((2048 // d, 7168), rng_for(seed, 1), 0.02),
             "out": "bf16",
         }
     if name == "mlp_down":

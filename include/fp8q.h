@@ -100,6 +100,23 @@ FP8Q_API int fp8q_quant_act_1x128(const void* x, int in_dtype, int64_t M, int64_
 FP8Q_API int fp8q_swiglu_quant_1x128(const void* gate, const void* up, int in_dtype, int64_t M,
                          int64_t I, int64_t ld, uint8_t* q, float* s, fp8q_stream_t stream);
 
+/* Fused RMSNorm + 1x128 FP8 cast: y = x * w / sqrt(mean_k x^2 + eps) per row,
+ * computed in FP32 and quantized per 1x128 tile exactly like
+ * fp8q_quant_act_1x128, without y being written.  woojincopolymer post,
+ * para. 3 (layer normalization fused with the FP8 cast; RMSNorm is
+ * DeepSeek-V3's normalization).  The row's sum of squares is an FP32
+ * reduction, so results match a correctly rounded evaluation to within a few
+ * FP32 ulp of y before the cast, not bit for bit.
+ *   x   [M][K]  in_dtype, 16-byte aligned
+ *   w   [K]     in_dtype (per-channel weight), 16-byte aligned
+ *   eps         > 0 and finite (FP8Q_ERR_INVALID_ARG otherwise)
+ *   q   [M][K]  uint8 E4M3, 16-byte aligned
+ *   s   [K/128][M] float32, 4-byte aligned
+ * Requires M >= 1 (below 2^31), K a multiple of 128 and at most 16384
+ * (FP8Q_ERR_UNSUPPORTED_SHAPE otherwise). */
+FP8Q_API int fp8q_rmsnorm_quant_1x128(const void* x, const void* w, int in_dtype, int64_t M,
+                         int64_t K, float eps, uint8_t* q, float* s, fp8q_stream_t stream);
+
 /* Activations regrouped for the backward pass, one scale per 128x1 tile
  * (128 consecutive tokens of one channel), written transposed so that the
  * result is a K-major GEMM operand whose K runs over tokens:

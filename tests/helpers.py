@@ -1,5 +1,5 @@
-"""Shared helpers for the parity tests: moving seeded numpy inputs to the GPU
-and the GEMM tolerance.
+"""Shared helpers for the parity tests: moving seeded numpy inputs to the GPU,
+the GEMM tolerance, and the check of the fused FP32-evaluated casts.
 
 Tolerance (the bar stated for this path): FP32 output
 |C - C_ref| <= 1e-5 * sum_k |a_k b_k|; BF16 output adds one BF16 unit in the
@@ -50,3 +50,39 @@ def cpu(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.bfloat16:
         return t.float().cpu().numpy()
     return t.cpu().numpy()
+
+
+def exact_scaled_1x128(h: np.ndarray) -> np.ndarray:
+    """h (FP64, [M][K], K a multiple of 128) -> h * inv of its 1x128 tile, inv
+    as the 1x128 rule makes it from the FP32-rounded values (amax 0 -> 1;
+    an overflowing inverse clamped to the largest float)."""
+    M, K = h.shape
+    h32 = h.astype(np.float32)
+    amax = np.abs(h32).reshape(M, K // 128, 128).max(axis=2)
+    with np.errstate(divide="ignore", over="ignore"):
+        inv = np.where(amax == 0, np.float32(1.0), np.float32(448.0) / amax).astype(np.float32)
+    inv = np.where(np.isinf(inv), np.finfo(np.float32).max, inv)
+    return h * np.repeat(inv.astype(np.float64), 128, axis=1)
+
+
+def check_fused_1x128(oracle, q_gpu, s_gpu, h, q_o, s_o, h_rel, s_rel, what):
+    """A fused operator + 1x128 cast evaluated in FP32 against the oracle's
+    exact operator (h, FP64) and its quantization (q_o, s_o):
+      * scales within s_rel relative;
+      * every code the round-to-nearest-even E4M3 encoding of some value
+        within h_rel relative of the exact scaled value h * inv (at a rounding
+        boundary either neighbour passes, anywhere else only one code);
+      * at least 99.9 % of the codes identical to the oracle's."""
+    s_gpu = np.asarray(s_gpu, np.float64)
+    rel = np.abs(s_gpu / np.asarray(s_o, np.float64) - 1.0)
+    assert rel.max() <= s_rel, "%s: scale off by %.3g relative" % (what, rel.max())
+    y = exact_scaled_1x128(h)
+    ends = [oracle.e4m3_decode(oracle.e4m3_encode((y * (1.0 + e)).astype(np.float32)))
+            for e in (-h_rel, h_rel)]
+    lo, hi = np.minimum(ends[0], ends[1]), np.maximum(ends[0], ends[1])
+    d = oracle.e4m3_decode(np.asarray(q_gpu))
+    bad = np.argwhere((d < lo) | (d > hi))
+    assert bad.size == 0, "%s: %d codes outside the interval, first at %s (gpu %r, allowed %r..%r)" % (
+        what, len(bad), tuple(bad[0]), d[tuple(bad[0])], lo[tuple(bad[0])], hi[tuple(bad[0])])
+    same = np.mean(np.asarray(q_gpu) == q_o)
+    assert same >= 0.999, "%s: only %.4f of codes equal the oracle's" % (what, same)

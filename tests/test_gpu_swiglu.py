@@ -18,7 +18,7 @@ import pytest
 import torch
 
 import fp8q_inputs as fi
-from helpers import cpu, to_dev
+from helpers import check_fused_1x128, cpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -34,33 +34,9 @@ def fq():
     return m
 
 
-def exact_scaled(oracle, h):
-    """h (FP64, [M][I]) -> h * inv of its tile, inv as the 1x128 rule makes it
-    from the FP32-rounded values (amax 0 -> 1; overflow clamped)."""
-    M, I = h.shape
-    h32 = h.astype(np.float32)
-    amax = np.abs(h32).reshape(M, I // 128, 128).max(axis=2)
-    with np.errstate(divide="ignore", over="ignore"):
-        inv = np.where(amax == 0, np.float32(1.0), np.float32(448.0) / amax).astype(np.float32)
-    inv = np.where(np.isinf(inv), np.finfo(np.float32).max, inv)
-    return h * np.repeat(inv.astype(np.float64), 128, axis=1)
-
-
 def check(oracle, q_gpu, s_gpu, g, u, what):
     q_o, s_o, h = oracle.swiglu_quant_1x128(g, u)
-    s_gpu = np.asarray(s_gpu, np.float64)
-    rel = np.abs(s_gpu / s_o.astype(np.float64) - 1.0)
-    assert rel.max() <= S_REL, "%s: scale off by %.3g relative" % (what, rel.max())
-    y = exact_scaled(oracle, h)
-    ends = [oracle.e4m3_decode(oracle.e4m3_encode((y * (1.0 + e)).astype(np.float32)))
-            for e in (-H_REL, H_REL)]
-    lo, hi = np.minimum(ends[0], ends[1]), np.maximum(ends[0], ends[1])
-    d = oracle.e4m3_decode(np.asarray(q_gpu))
-    bad = np.argwhere((d < lo) | (d > hi))
-    assert bad.size == 0, "%s: %d codes outside the interval, first at %s (gpu %r, allowed %r..%r)" % (
-        what, len(bad), tuple(bad[0]), d[tuple(bad[0])], lo[tuple(bad[0])], hi[tuple(bad[0])])
-    same = np.mean(np.asarray(q_gpu) == q_o)
-    assert same >= 0.999, "%s: only %.4f of codes equal the oracle's" % (what, same)
+    check_fused_1x128(oracle, q_gpu, s_gpu, h, q_o, s_o, H_REL, S_REL, what)
     return q_o, s_o
 
 
