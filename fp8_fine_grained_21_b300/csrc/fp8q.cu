@@ -323,15 +323,30 @@ int fp8q_rmsnorm_quant_1x128(const void* x, const void* w, int in_dtype, int64_t
     if (K % 128 || K > kRnMaxK || M > 0x7fffffff) return FP8Q_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(x, 16) || !aligned(w, 16) || !aligned(q, 16) || !aligned(s, 4))
         return FP8Q_ERR_MISALIGNED;
-    const unsigned threads = static_cast<unsigned>((K / 16 + 31) / 32 * 32);
+    DeviceState* d = nullptr;
+    const int rc = device_state(&d);
+    if (rc != FP8Q_OK) return rc;
+    const int threads = static_cast<int>((K / 16 + 31) / 32 * 32);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (in_dtype == FP8Q_BF16)
-        k_rmsnorm_quant_1x128<__nv_bfloat16><<<static_cast<unsigned>(M), threads, 0, st>>>(
+    // persistent: as many CTAs as fit on the GPU at once (at most one per row)
+    auto grid_for = [&](const void* kern) -> unsigned {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        const int64_t g = static_cast<int64_t>(per_sm) * d->num_sms;
+        return static_cast<unsigned>(g < M ? g : M);
+    };
+    if (in_dtype == FP8Q_BF16) {
+        auto kern = k_rmsnorm_quant_1x128<__nv_bfloat16>;
+        kern<<<grid_for(reinterpret_cast<const void*>(kern)), threads, 0, st>>>(
             static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w), M, K, eps,
             q, s);
-    else
-        k_rmsnorm_quant_1x128<float><<<static_cast<unsigned>(M), threads, 0, st>>>(
+    } else {
+        auto kern = k_rmsnorm_quant_1x128<float>;
+        kern<<<grid_for(reinterpret_cast<const void*>(kern)), threads, 0, st>>>(
             static_cast<const float*>(x), static_cast<const float*>(w), M, K, eps, q, s);
+    }
     return launched();
 }
 

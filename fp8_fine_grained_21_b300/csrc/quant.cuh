@@ -279,36 +279,73 @@ __global__ void __launch_bounds__(256, 6) k_swiglu_quant_1x128(const T* __restri
 // ----------------------------------------------- RMSNorm + 1x128 FP8 cast
 // Layer normalization fused with the FP8 cast (woojincopolymer post, para.
 // 3); DeepSeek-V3's normalization is RMSNorm: y = x w / sqrt(mean(x^2) + eps)
-// per row.  One CTA per row, K/16 threads rounded up to whole warps, each
-// holding 16 consecutive elements in registers from the load to the store:
-// the row's sum of squares goes through warp shuffles and one shared-memory
-// step, r = 1/sqrt(mean + eps) is correctly rounded, y = (x r) w, and eight
-// threads (128 elements) form a 1x128 tile with the scale rule and cast of
-// k_quant_1x128.  FP32 throughout, so y differs from an exact evaluation by
-// the summation's rounding (a few FP32 ulp of the mean).
+// per row.  A persistent grid of CTAs with K/16 threads each (rounded up to
+// whole warps); a CTA walks rows blockIdx.x, +gridDim.x, ..., and each thread
+// keeps 16 consecutive elements of its row in registers from the load to the
+// store, with the next row's 16 elements already loading while the current
+// row is reduced and stored (the weights are re-read per row, from L1).  The row's sum of squares goes through warp
+// shuffles and one shared-memory step, r = 1/sqrt(mean + eps) is correctly
+// rounded, y = (x r) w, and eight threads (128 elements) form a 1x128 tile
+// with the scale rule and cast of k_quant_1x128.  FP32 throughout, so y
+// differs from an exact evaluation by the summation's rounding (a few FP32
+// ulp of the mean).
 constexpr int kRnMaxK = 16384;       // 1024 threads x 16 elements
 
-__device__ __forceinline__ void load16(const __nv_bfloat16* p, float (&v)[16]) {
-    float a[8], b[8];
-    load8(p, a);
-    load8(p + 8, b);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        v[i] = a[i];
-        v[8 + i] = b[i];
-    }
-}
+// Sixteen consecutive elements kept in their storage format until used.
+template <typename T>
+struct Raw16;
 
-__device__ __forceinline__ void load16(const float* p, float (&v)[16]) {
-    float a[8], b[8];
-    load8(p, a);
-    load8(p + 8, b);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        v[i] = a[i];
-        v[8 + i] = b[i];
+template <>
+struct Raw16<__nv_bfloat16> {
+    uint4 a, b;
+    __device__ void zero() { a = b = make_uint4(0u, 0u, 0u, 0u); }
+    __device__ void stream(const __nv_bfloat16* p) {
+        a = __ldcs(reinterpret_cast<const uint4*>(p));
+        b = __ldcs(reinterpret_cast<const uint4*>(p) + 1);
     }
-}
+    __device__ void keep(const __nv_bfloat16* p) {
+        a = __ldg(reinterpret_cast<const uint4*>(p));
+        b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+    }
+    __device__ void to_f32(float (&v)[16]) const {
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+};
+
+template <>
+struct Raw16<float> {
+    float4 a, b, c, d;
+    __device__ void zero() { a = b = c = d = make_float4(0.f, 0.f, 0.f, 0.f); }
+    __device__ void stream(const float* p) {
+        const float4* q = reinterpret_cast<const float4*>(p);
+        a = __ldcs(q);
+        b = __ldcs(q + 1);
+        c = __ldcs(q + 2);
+        d = __ldcs(q + 3);
+    }
+    __device__ void keep(const float* p) {
+        const float4* q = reinterpret_cast<const float4*>(p);
+        a = __ldg(q);
+        b = __ldg(q + 1);
+        c = __ldg(q + 2);
+        d = __ldg(q + 3);
+    }
+    __device__ void to_f32(float (&v)[16]) const {
+        const float4 f[4] = {a, b, c, d};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[4 * i] = f[i].x;
+            v[4 * i + 1] = f[i].y;
+            v[4 * i + 2] = f[i].z;
+            v[4 * i + 3] = f[i].w;
+        }
+    }
+};
 
 template <typename T>
 __global__ void __launch_bounds__(1024) k_rmsnorm_quant_1x128(const T* __restrict__ x,
@@ -318,56 +355,67 @@ __global__ void __launch_bounds__(1024) k_rmsnorm_quant_1x128(const T* __restric
                                                               float* __restrict__ s) {
     __shared__ float red[32];
     __shared__ float total;
-    const int64_t m = blockIdx.x;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int nwarps = blockDim.x >> 5;
     const int64_t k0 = static_cast<int64_t>(t) * 16;
     const bool live = k0 < K;
-    float v[16], wv[16];
-    float ss = 0.0f;
-    if (live) {
-        load16(x + m * K + k0, v);
-        load16(w + k0, wv);
+    Raw16<T> cur, nxt;
+    cur.zero();
+    nxt.zero();
+    int64_t m = blockIdx.x;
+    if (live && m < M) cur.stream(x + m * K + k0);
+#pragma unroll 1
+    for (; m < M; m += gridDim.x) {
+        const int64_t mn = m + gridDim.x;
+        if (live && mn < M) nxt.stream(x + mn * K + k0);
+        float v[16];
+        cur.to_f32(v);
+        float ss = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) ss = __fmaf_rn(v[i], v[i], ss);
-    } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = wv[i] = 0.0f;
-    }
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        if (warp == 0) {
+            float a = lane < nwarps ? red[lane] : 0.0f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    if (warp == 0) {
-        float a = lane < nwarps ? red[lane] : 0.0f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-        if (lane == 0) total = a;
-    }
-    __syncthreads();
-    const float r = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, static_cast<float>(K)), eps));
-    float a = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        v[i] = __fmul_rn(__fmul_rn(v[i], r), wv[i]);
-        a = fmaxf(a, fabsf(v[i]));
-    }
-    // a 1x128 tile is eight consecutive threads (lanes 8j .. 8j+7 of a warp)
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    float sc, inv;
-    group_scale(a, sc, inv);
-    if (live) {
-        float lo[8], hi[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            lo[i] = v[i];
-            hi[i] = v[8 + i];
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            if (lane == 0) total = a;
         }
-        const uint2 p0 = quant8(lo, inv), p1 = quant8(hi, inv);
-        *reinterpret_cast<uint4*>(q + m * K + k0) = make_uint4(p0.x, p0.y, p1.x, p1.y);
-        if ((t & 7) == 0) s[(k0 / 128) * M + m] = sc;
+        __syncthreads();
+        const float r = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, static_cast<float>(K)), eps));
+        float wv[16];
+        {
+            Raw16<T> wr;                 // the weights, re-read per row from L1
+            wr.zero();
+            if (live) wr.keep(w + k0);
+            wr.to_f32(wv);
+        }
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            v[i] = __fmul_rn(__fmul_rn(v[i], r), wv[i]);
+            a = fmaxf(a, fabsf(v[i]));
+        }
+        // a 1x128 tile is eight consecutive threads (lanes 8j .. 8j+7 of a warp)
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        float sc, inv;
+        group_scale(a, sc, inv);
+        if (live) {
+            float lo[8], hi[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                lo[i] = v[i];
+                hi[i] = v[8 + i];
+            }
+            const uint2 p0 = quant8(lo, inv), p1 = quant8(hi, inv);
+            *reinterpret_cast<uint4*>(q + m * K + k0) = make_uint4(p0.x, p0.y, p1.x, p1.y);
+            if ((t & 7) == 0) s[(k0 / 128) * M + m] = sc;
+        }
+        cur = nxt;
     }
 }
 

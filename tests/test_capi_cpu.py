@@ -76,6 +76,17 @@ def test_quant_argument_checks(lib):
     assert h(A16, 0, 128, 128, MIS, A16c, None) == 3
 
 
+def test_rmsnorm_quant_argument_checks(lib):
+    f = lib.fp8q_rmsnorm_quant_1x128
+    f.argtypes = [P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, P, P, P]
+    assert f(A16, None, 1, 64, 256, 1e-6, A16b, A16c, None) == 1       # null weight
+    assert f(A16, A16, 1, 64, 256, 0.0, A16b, A16c, None) == 1         # eps must be > 0
+    assert f(A16, A16, 1, 64, 256, float("nan"), A16b, A16c, None) == 1
+    assert f(A16, A16, 1, 64, 200, 1e-6, A16b, A16c, None) == 2        # K not a multiple of 128
+    assert f(A16, A16, 1, 64, 16384 + 128, 1e-6, A16b, A16c, None) == 2   # K above 16384
+    assert f(MIS, A16, 1, 64, 256, 1e-6, A16b, A16c, None) == 3        # misaligned input
+
+
 def test_swiglu_quant_argument_checks(lib):
     f = lib.fp8q_swiglu_quant_1x128
     assert f(None, A16, 1, 64, 256, 512, A16b, A16c, None) == 1     # null gate
