@@ -220,6 +220,8 @@ int gemm_common(const uint8_t* A8, const float* sA, const uint8_t* B8, const flo
     if (M > (int64_t(1) << 30) || N > (int64_t(1) << 24) || K > (int64_t(1) << 30))
         return FP8Q_ERR_UNSUPPORTED_SHAPE;
     if (int64_t(G) * N > (int64_t(1) << 31) - 1) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    // output tiles are counted in 32-bit integers on the device
+    if ((M / 128) * (N / 128) > (int64_t(1) << 31) - 1) return FP8Q_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(A8, 16) || !aligned(B8, 16) || !aligned(sA, 16) || !aligned(C, 16))
         return FP8Q_ERR_MISALIGNED;
     if (!aligned(sB, bscale == FP8Q_BSCALE_ROW1x128 ? 16 : 4)) return FP8Q_ERR_MISALIGNED;

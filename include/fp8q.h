@@ -171,7 +171,9 @@ FP8Q_API int fp8q_transpose_w_128x128(const uint8_t* q, const float* s, int64_t 
  *   B8  [N][K]  uint8 E4M3, 16-byte aligned     sB [N/128][K/128] float32
  *   C   [M][N]  out_dtype (FP8Q_F32 or FP8Q_BF16, BF16 rounded to nearest even),
  *               16-byte aligned; fully overwritten.
- * Requires M, N, K multiples of 128.  Runs on the legacy default stream. */
+ * Requires M, N, K multiples of 128, M and K at most 2^30, N at most 2^24 and
+ * at most 2^31 - 1 output tiles of 128 x 128 (FP8Q_ERR_UNSUPPORTED_SHAPE
+ * otherwise).  Runs on the legacy default stream. */
 FP8Q_API int fp8q_gemm(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,
               void* C, int64_t M, int64_t N, int64_t K, int out_dtype);
 

@@ -109,6 +109,7 @@ def test_gemm_argument_checks(lib):
     assert g(*ok, 128, 128, 64, 0, 0, None) == 2                # ragged K
     assert g(*ok, -128, 128, 128, 0, 0, None) == 1
     assert g(MIS, *ok[1:], 128, 128, 128, 0, 0, None) == 3
+    assert g(*ok, 1 << 30, 1 << 24, 128, 0, 0, None) == 2       # 2^37 output tiles
     gg = lib.fp8q_gemm_grouped
     assert gg(*ok, None, 4, 512, 128, 128, 1, None) == 1       # no offsets
     assert gg(*ok, A16, 0, 512, 128, 128, 1, None) == 2        # no groups
