@@ -623,6 +623,8 @@ def run_fp8q(args):
         "gemm_frac_of_fp8_peak": gemm_tflops / fp8_peak,
         "quant_gbs": q_gbs,
         "quant_frac_of_hbm": [q / peaks["hbm_gbs"] for q in q_gbs],
+        # the same against the ~8 TB/s nominal HBM3e figure, for context
+        "quant_frac_of_nominal_hbm_8tbs": [q / 8000.0 for q in q_gbs],
         # the same quantizers launched back to back over copies of their input
         # (together 3x L2), ramp and tail amortised; null for inputs >= 256 MB
         "quant_back_to_back": [None if b is None else {
