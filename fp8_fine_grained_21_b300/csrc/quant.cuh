@@ -7,6 +7,13 @@
 // block.  Scaling ("online quantization" section; para. 1 of "Six
 // Reasons..."): the group's largest magnitude maps onto 448, the largest
 // finite E4M3 value, computed from the data at hand (no history).
+//
+// Contents: the shared scale rule and cast; k_quant_1x128 (direct loads,
+// many short CTAs); k_swiglu_quant_1x128 and k_rmsnorm_quant_1x128 (the cast
+// fused into the operator that produces the activation, woojincopolymer
+// post, paras. 3-4); k_quant_128x128 and k_quant_128x1 (persistent, TMA
+// stage ring); the backward-pass regrouping of stored 1x128 tiles into 128x1
+// tiles and the FP8 weight transpose.
 #pragma once
 
 #include <cfloat>
