@@ -8,7 +8,9 @@
  *   codingmall.com knowledge-base article on FP8 in DeepSeek-V3 (Greek),
  *     sections "fine-grained quantization", "online quantization",
  *     "increased accumulation precision", "unified E4M3 format";
- *   codingmall.com article on FP8 GEMM in DeepSeek-V3 (Japanese), items 1-8.
+ *   codingmall.com article on FP8 GEMM in DeepSeek-V3 (Japanese), items 1-8;
+ *   woojincopolymer.co.kr board post, paras. 3-4 (the FP8 cast fused into the
+ *     operator that produces the activation: RMSNorm, SwiGLU).
  *
  * Conventions shared by every call
  * --------------------------------
