@@ -20,7 +20,8 @@ __all__ = [
     "transpose_w_128x128",
     "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_gemm_ws", "fp8q_gemm_grouped_ws",
     "fp8q_gemm_workspace_size", "fp8q_gemm_noalloc", "fp8q_get_device_status",
-    "fp8q_selftest_wait", "fp8q_status_string", "fp8q_version", "workspace",
+    "fp8q_selftest_wait", "fp8q_bench_mma_peak", "fp8q_num_sms", "fp8q_status_string",
+    "fp8q_version", "workspace",
     "quant_act_1x128", "quant_act_128x1", "quant_w_128x128", "gemm", "gemm_grouped",
     "F32", "BF16", "BSCALE_BLOCK128", "BSCALE_ROW1x128",
 ]
@@ -38,7 +39,8 @@ EXPORTS = ("fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128
            "fp8q_retile_1x128_to_128x1", "fp8q_transpose_w_128x128", "fp8q_gemm",
            "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_gemm_ws", "fp8q_gemm_grouped_ws",
            "fp8q_gemm_workspace_size", "fp8q_gemm_noalloc", "fp8q_get_device_status",
-           "fp8q_selftest_wait", "fp8q_status_string", "fp8q_version")
+           "fp8q_selftest_wait", "fp8q_bench_mma_peak", "fp8q_num_sms", "fp8q_status_string",
+           "fp8q_version")
 
 
 class Fp8qError(RuntimeError):
@@ -93,6 +95,10 @@ def load():
     lib.fp8q_gemm_noalloc.restype = I
     lib.fp8q_selftest_wait.argtypes = [I64, P]
     lib.fp8q_selftest_wait.restype = I
+    lib.fp8q_bench_mma_peak.argtypes = [I64, P]
+    lib.fp8q_bench_mma_peak.restype = I
+    lib.fp8q_num_sms.argtypes = []
+    lib.fp8q_num_sms.restype = I
     lib.fp8q_get_device_status.argtypes = [P]
     lib.fp8q_get_device_status.restype = I
     lib.fp8q_status_string.argtypes = [I]
@@ -147,9 +153,61 @@ def _out_dtype(dt):
     raise ValueError("output must be float32 or bfloat16, got %s" % dt)
 
 
+def _shape(t, name, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def _numel(t, name, n):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.numel() != n:
+        raise ValueError("%s must hold %d elements, got %d" % (name, n, t.numel()))
+
+
+def _gemm_dims(A8, B8, C, sA, sB, bscale, grouped=False):
+    """(M, N, K[, G]) of a GEMM call, after checking that every buffer has the
+    size the library will read or write: A8 [M][K]; B8 [N][K] ([G][N][K]
+    grouped); C [M][N]; sA [K/128][M]; sB [N/128][K/128] ([G][..] grouped) for
+    128x128 blocks or [K/128][N] for 1x128 rows.  The library trusts these
+    sizes, so a mismatch here would otherwise read or write out of bounds."""
+    if A8.dim() != 2:
+        raise ValueError("A8 must be 2-D [M][K]")
+    M, K = A8.shape
+    if grouped:
+        if B8.dim() != 3:
+            raise ValueError("B8 must be 3-D [G][N][K]")
+        G, N, Kb_ = B8.shape
+    else:
+        if B8.dim() != 2:
+            raise ValueError("B8 must be 2-D [N][K]")
+        G = 1
+        N, Kb_ = B8.shape
+    if Kb_ != K:
+        raise ValueError("A8 and B8 must have the same K (%d vs %d)" % (K, Kb_))
+    _shape(C, "C", (M, N))
+    kb, nb = _scales(K), _scales(N)
+    _numel(sA, "sA", kb * M)
+    if bscale == BSCALE_ROW1x128:
+        _numel(sB, "sB", kb * N)
+    elif bscale == BSCALE_BLOCK128:
+        _numel(sB, "sB", G * nb * kb)
+    else:
+        raise ValueError("bscale must be BSCALE_BLOCK128 or BSCALE_ROW1x128")
+    return (M, N, K, G) if grouped else (M, N, K)
+
+
+def _quant_out(q, s, q_shape, s_numel):
+    _shape(q, "q", q_shape)
+    _numel(s, "s", s_numel)
+
+
 # ------------------------------------------------------- same-name bindings
 def fp8q_quant_act_1x128(x, q, s, stream=None):
     M, K = x.shape
+    _quant_out(q, s, (M, K), _scales(K) * M)
     _check("fp8q_quant_act_1x128", load().fp8q_quant_act_1x128(
         _dev(x, "x"), _in_dtype(x), M, K, _dev(q, "q", torch.uint8),
         _dev(s, "s", torch.float32), _stream(stream)))
@@ -176,6 +234,7 @@ def fp8q_swiglu_quant_1x128(gate, up, q, s, stream=None):
     if ldu != ld:
         raise ValueError("gate and up must have the same row stride")
     M, I = gate.shape
+    _quant_out(q, s, (M, I), _scales(I) * M)
     _check("fp8q_swiglu_quant_1x128", load().fp8q_swiglu_quant_1x128(
         pg, pu, _in_dtype(gate), M, I, ld, _dev(q, "q", torch.uint8),
         _dev(s, "s", torch.float32), _stream(stream)))
@@ -186,6 +245,7 @@ def fp8q_rmsnorm_quant_1x128(x, w, q, s, eps=1e-6, stream=None):
     M, K = x.shape
     if w.dtype != x.dtype or tuple(w.shape) != (K,):
         raise ValueError("w must be [K] with x's dtype")
+    _quant_out(q, s, (M, K), _scales(K) * M)
     _check("fp8q_rmsnorm_quant_1x128", load().fp8q_rmsnorm_quant_1x128(
         _dev(x, "x"), _dev(w, "w"), _in_dtype(x), M, K, ctypes.c_float(eps),
         _dev(q, "q", torch.uint8), _dev(s, "s", torch.float32), _stream(stream)))
@@ -193,6 +253,8 @@ def fp8q_rmsnorm_quant_1x128(x, w, q, s, eps=1e-6, stream=None):
 
 def fp8q_quant_act_128x1(x, qT, sT, stream=None):
     T, C = x.shape
+    _shape(qT, "qT", (C, T))
+    _numel(sT, "sT", _scales(T) * C)
     _check("fp8q_quant_act_128x1", load().fp8q_quant_act_128x1(
         _dev(x, "x"), _in_dtype(x), T, C, _dev(qT, "qT", torch.uint8),
         _dev(sT, "sT", torch.float32), _stream(stream)))
@@ -200,6 +262,7 @@ def fp8q_quant_act_128x1(x, qT, sT, stream=None):
 
 def fp8q_quant_w_128x128(w, q, s, stream=None):
     N, K = w.shape
+    _quant_out(q, s, (N, K), _scales(N) * _scales(K))
     _check("fp8q_quant_w_128x128", load().fp8q_quant_w_128x128(
         _dev(w, "w"), _in_dtype(w), N, K, _dev(q, "q", torch.uint8),
         _dev(s, "s", torch.float32), _stream(stream)))
@@ -207,6 +270,9 @@ def fp8q_quant_w_128x128(w, q, s, stream=None):
 
 def fp8q_retile_1x128_to_128x1(q, s, qT, sT, stream=None):
     T, C = q.shape
+    _numel(s, "s", _scales(C) * T)
+    _shape(qT, "qT", (C, T))
+    _numel(sT, "sT", _scales(T) * C)
     _check("fp8q_retile_1x128_to_128x1", load().fp8q_retile_1x128_to_128x1(
         _dev(q, "q", torch.uint8), _dev(s, "s", torch.float32), T, C, _dev(qT, "qT", torch.uint8),
         _dev(sT, "sT", torch.float32), _stream(stream)))
@@ -214,22 +280,23 @@ def fp8q_retile_1x128_to_128x1(q, s, qT, sT, stream=None):
 
 def fp8q_transpose_w_128x128(q, s, qT, sT, stream=None):
     N, K = q.shape
+    _numel(s, "s", _scales(N) * _scales(K))
+    _shape(qT, "qT", (K, N))
+    _numel(sT, "sT", _scales(K) * _scales(N))
     _check("fp8q_transpose_w_128x128", load().fp8q_transpose_w_128x128(
         _dev(q, "q", torch.uint8), _dev(s, "s", torch.float32), N, K, _dev(qT, "qT", torch.uint8),
         _dev(sT, "sT", torch.float32), _stream(stream)))
 
 
 def fp8q_gemm(A8, sA, B8, sB, C):
-    M, K = A8.shape
-    N = B8.shape[0]
+    M, N, K = _gemm_dims(A8, B8, C, sA, sB, BSCALE_BLOCK128)
     _check("fp8q_gemm", load().fp8q_gemm(
         _dev(A8, "A8", torch.uint8), _dev(sA, "sA", torch.float32), _dev(B8, "B8", torch.uint8),
         _dev(sB, "sB", torch.float32), _dev(C, "C"), M, N, K, _out_dtype(C.dtype)))
 
 
 def fp8q_gemm_ex(A8, sA, B8, sB, C, bscale=BSCALE_BLOCK128, stream=None):
-    M, K = A8.shape
-    N = B8.shape[0]
+    M, N, K = _gemm_dims(A8, B8, C, sA, sB, bscale)
     _check("fp8q_gemm_ex", load().fp8q_gemm_ex(
         _dev(A8, "A8", torch.uint8), _dev(sA, "sA", torch.float32), _dev(B8, "B8", torch.uint8),
         _dev(sB, "sB", torch.float32), _dev(C, "C"), M, N, K, _out_dtype(C.dtype), int(bscale),
@@ -237,8 +304,8 @@ def fp8q_gemm_ex(A8, sA, B8, sB, C, bscale=BSCALE_BLOCK128, stream=None):
 
 
 def fp8q_gemm_grouped(A8, sA, B8, sB, C, m_offsets, stream=None):
-    Mtot, K = A8.shape
-    G, N, _ = B8.shape
+    Mtot, N, K, G = _gemm_dims(A8, B8, C, sA, sB, BSCALE_BLOCK128, grouped=True)
+    _numel(m_offsets, "m_offsets", G + 1)
     _check("fp8q_gemm_grouped", load().fp8q_gemm_grouped(
         _dev(A8, "A8", torch.uint8), _dev(sA, "sA", torch.float32), _dev(B8, "B8", torch.uint8),
         _dev(sB, "sB", torch.float32), _dev(C, "C"), _dev(m_offsets, "m_offsets", torch.int32),
@@ -252,8 +319,7 @@ def _ws(ws):
 
 
 def fp8q_gemm_ws(A8, sA, B8, sB, C, bscale=BSCALE_BLOCK128, ws=None, stream=None):
-    M, K = A8.shape
-    N = B8.shape[0]
+    M, N, K = _gemm_dims(A8, B8, C, sA, sB, bscale)
     wp, wn = _ws(ws)
     _check("fp8q_gemm_ws", load().fp8q_gemm_ws(
         _dev(A8, "A8", torch.uint8), _dev(sA, "sA", torch.float32), _dev(B8, "B8", torch.uint8),
@@ -262,8 +328,8 @@ def fp8q_gemm_ws(A8, sA, B8, sB, C, bscale=BSCALE_BLOCK128, ws=None, stream=None
 
 
 def fp8q_gemm_grouped_ws(A8, sA, B8, sB, C, m_offsets, ws=None, stream=None):
-    Mtot, K = A8.shape
-    G, N, _ = B8.shape
+    Mtot, N, K, G = _gemm_dims(A8, B8, C, sA, sB, BSCALE_BLOCK128, grouped=True)
+    _numel(m_offsets, "m_offsets", G + 1)
     wp, wn = _ws(ws)
     _check("fp8q_gemm_grouped_ws", load().fp8q_gemm_grouped_ws(
         _dev(A8, "A8", torch.uint8), _dev(sA, "sA", torch.float32), _dev(B8, "B8", torch.uint8),
@@ -273,8 +339,7 @@ def fp8q_gemm_grouped_ws(A8, sA, B8, sB, C, m_offsets, ws=None, stream=None):
 
 def fp8q_gemm_noalloc(A8, sA, B8, sB, C, bscale=BSCALE_BLOCK128, stream=None):
     """The stream-K GEMM on the library's own scratch array (no allocation)."""
-    M, K = A8.shape
-    N = B8.shape[0]
+    M, N, K = _gemm_dims(A8, B8, C, sA, sB, bscale)
     _check("fp8q_gemm_noalloc", load().fp8q_gemm_noalloc(
         _dev(A8, "A8", torch.uint8), _dev(sA, "sA", torch.float32), _dev(B8, "B8", torch.uint8),
         _dev(sB, "sB", torch.float32), _dev(C, "C"), M, N, K, _out_dtype(C.dtype), int(bscale),
@@ -312,6 +377,17 @@ def fp8q_get_device_status(stream=None) -> int:
 
 def fp8q_selftest_wait(limit_ns: int, stream=None):
     _check("fp8q_selftest_wait", load().fp8q_selftest_wait(int(limit_ns), _stream(stream)))
+
+
+def fp8q_bench_mma_peak(blocks: int, stream=None):
+    _check("fp8q_bench_mma_peak", load().fp8q_bench_mma_peak(int(blocks), _stream(stream)))
+
+
+def fp8q_num_sms() -> int:
+    n = int(load().fp8q_num_sms())
+    if n <= 0:
+        raise Fp8qError("fp8q_num_sms", -n)
+    return n
 
 
 def fp8q_status_string(status: int) -> str:

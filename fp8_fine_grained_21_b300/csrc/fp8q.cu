@@ -1,7 +1,10 @@
 // C ABI of the fp8q library (declared in include/fp8q.h): argument checks,
 // TMA descriptor encoding and kernel launches.  No allocation happens here:
-// every buffer belongs to the caller; the only library state is a per-device
-// status word (a static __device__ variable) and cached launch attributes.
+// every buffer belongs to the caller.  Library state: a per-device status
+// word (a static __device__ variable), cached launch attributes, and
+// g_noalloc_scratch, the 40 MiB static device array that fp8q_gemm_noalloc
+// uses as its stream-K workspace (one array per device, shared by every call
+// of that entry point: calls that overlap on the GPU race).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -42,6 +45,65 @@ __global__ void k_selftest_wait(int* status, uint64_t limit_ns) {
     (void)done;
 }
 
+// Tensor-pipe throughput probe (a measurement, not part of the method): one
+// CTA per SM issues `blocks` x 4 MMAs of 128 x 256 x 32 E4M3 -> FP32 (one
+// 128-element K block each) from fixed shared-memory operands into one TMEM
+// accumulator, back to back, and waits for them with a bounded wait.  The
+// operand bytes are a fixed pseudo-random pattern of finite E4M3 values, so
+// the tensor cores see data of realistic bit density, not zeros.
+constexpr int kPeakN = 256;
+constexpr int kPeakSmem = kBM * kBK + kPeakN * kBK + 1024;
+
+__global__ void __launch_bounds__(128, 1) k_mma_peak(int64_t blocks, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t done;
+    __shared__ uint32_t tbase;
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    constexpr int kBytes = kBM * kBK + kPeakN * kBK;
+    for (int i = threadIdx.x; i < kBytes / 4; i += blockDim.x) {
+        uint32_t h = static_cast<uint32_t>(i) * 0x9E3779B1u + blockIdx.x * 0x85EBCA6Bu;
+        h ^= h >> 15;
+        h *= 0x2C1B3C6Du;
+        h ^= h >> 12;
+        // clearing bit 3 of every byte keeps it off the NaN patterns 0x7F / 0xFF
+        reinterpret_cast<uint32_t*>(smem)[i] = h & 0x77777777u;
+    }
+    fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
+        mbar_init(&done, 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x < 32) {
+        tmem_alloc(&tbase, kPeakN);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x == 0) {
+        constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, kPeakN);
+        const uint32_t a_addr = smem_u32(smem);
+        const uint64_t ad = sw128_desc(a_addr);
+        const uint64_t bd = sw128_desc(a_addr + kBM * kBK);
+#pragma unroll 1
+        for (int64_t b = 0; b < blocks; ++b) {
+#pragma unroll
+            for (int k = 0; k < kBK / 32; ++k)
+                mma_e4m3(tbase, ad + 2 * k, bd + 2 * k, kIdesc, (b > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(&done);
+        if (!mbar_drain(&done, 0, kWaitLimitNs)) atomicCAS(status, kOk, kErrTimeout);
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        tc_fence_after();
+        tmem_dealloc(tbase, kPeakN);
+    }
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -53,6 +115,7 @@ struct DeviceState {
     bool gemm_attr[2][2][2] = {};     // dynamic-smem attribute set, per kernel instance
     bool quant_attr[2][2] = {};       // the same for the staged quantizers [kind][bf16 input]
     uint8_t* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch
+    bool peak_attr = false;              // dynamic-smem attribute of k_mma_peak set
 };
 
 std::mutex g_mutex;
@@ -209,9 +272,21 @@ constexpr size_t kWsPartialBytes(int sms) {
     return static_cast<size_t>(2) * sms * (kBM * 256) * sizeof(float);
 }
 
-int gemm_common(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB, void* C,
-                const int* m_offsets, int G, int64_t M, int64_t N, int64_t K, int out_dtype,
-                int bscale, void* workspace, size_t ws_bytes, cudaStream_t st) {
+// Everything a GEMM launch needs, made by gemm_plan after every check has
+// passed; gemm_launch then only launches.
+struct GemmPlan {
+    DeviceState* d = nullptr;
+    CUtensorMap ta, tb;
+    GemmArgs args;
+    int BN = 256;
+    int tiles_upper = 1;
+    bool row_b = false, bf16 = false;
+};
+
+// Checks that need neither a device nor the SM count.
+int gemm_check_args(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,
+                    const void* C, int G, int64_t M, int64_t N, int64_t K, int out_dtype,
+                    int bscale) {
     if (!A8 || !sA || !B8 || !sB || !C) return FP8Q_ERR_INVALID_ARG;
     if (out_dtype != FP8Q_F32 && out_dtype != FP8Q_BF16) return FP8Q_ERR_INVALID_ARG;
     if (bscale != FP8Q_BSCALE_BLOCK128 && bscale != FP8Q_BSCALE_ROW1x128) return FP8Q_ERR_INVALID_ARG;
@@ -225,42 +300,61 @@ int gemm_common(const uint8_t* A8, const float* sA, const uint8_t* B8, const flo
     if (!aligned(A8, 16) || !aligned(B8, 16) || !aligned(sA, 16) || !aligned(C, 16))
         return FP8Q_ERR_MISALIGNED;
     if (!aligned(sB, bscale == FP8Q_BSCALE_ROW1x128 ? 16 : 4)) return FP8Q_ERR_MISALIGNED;
-    DeviceState* d = nullptr;
-    int rc = device_state(&d);
+    return FP8Q_OK;
+}
+
+int gemm_plan(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB, void* C,
+              const int* m_offsets, int G, int64_t M, int64_t N, int64_t K, int out_dtype,
+              int bscale, void* workspace, size_t ws_bytes, GemmPlan& p) {
+    int rc = gemm_check_args(A8, sA, B8, sB, C, G, M, N, K, out_dtype, bscale);
     if (rc != FP8Q_OK) return rc;
+    if ((rc = device_state(&p.d)) != FP8Q_OK) return rc;
     if (workspace) {
         if (!aligned(workspace, 256)) return FP8Q_ERR_MISALIGNED;
-        if (ws_bytes < kWsCounterBytes(d->num_sms) + kWsPartialBytes(d->num_sms))
+        if (ws_bytes < kWsCounterBytes(p.d->num_sms) + kWsPartialBytes(p.d->num_sms))
             return FP8Q_ERR_INVALID_ARG;
     }
-    const int BN = (N % 256 == 0) ? 256 : 128;
-    CUtensorMap ta, tb;
-    std::memset(&ta, 0, sizeof(ta));
-    std::memset(&tb, 0, sizeof(tb));
-    if ((rc = encode_kmajor(&ta, A8, K, M, 128)) != FP8Q_OK) return rc;
-    if ((rc = encode_kmajor(&tb, B8, K, int64_t(G) * N, BN)) != FP8Q_OK) return rc;
-    GemmArgs args;
-    args.sA = sA;
-    args.sB = sB;
-    args.C = C;
-    args.m_offsets = m_offsets;
-    args.M_total = static_cast<int>(M);
-    args.N = static_cast<int>(N);
-    args.K = static_cast<int>(K);
-    args.G = G;
-    args.status = d->status;
-    args.counters = workspace ? static_cast<int*>(workspace) : nullptr;
-    args.ws = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                                    kWsCounterBytes(d->num_sms))
-                        : nullptr;
-    const int64_t tiles = (M / 128) * (N / BN);
+    p.BN = (N % 256 == 0) ? 256 : 128;
+    std::memset(&p.ta, 0, sizeof(p.ta));
+    std::memset(&p.tb, 0, sizeof(p.tb));
+    if ((rc = encode_kmajor(&p.ta, A8, K, M, 128)) != FP8Q_OK) return rc;
+    if ((rc = encode_kmajor(&p.tb, B8, K, int64_t(G) * N, p.BN)) != FP8Q_OK) return rc;
+    GemmArgs& a = p.args;
+    a.sA = sA;
+    a.sB = sB;
+    a.C = C;
+    a.m_offsets = m_offsets;
+    a.M_total = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.G = G;
+    a.status = p.d->status;
+    a.counters = workspace ? static_cast<int*>(workspace) : nullptr;
+    a.ws = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                 kWsCounterBytes(p.d->num_sms))
+                     : nullptr;
+    const int64_t tiles = (M / 128) * (N / p.BN);
     // with a workspace every SM takes part (stream-K shares out the tail)
-    const int tiles_upper = workspace ? d->num_sms
-                            : tiles > (int64_t(1) << 30) ? (1 << 30) : static_cast<int>(tiles);
-    const bool row_b = bscale == FP8Q_BSCALE_ROW1x128;
-    const bool bf16 = out_dtype == FP8Q_BF16;
-    return BN == 256 ? launch_gemm_bn<256>(d, ta, tb, args, tiles_upper, row_b, bf16, st)
-                     : launch_gemm_bn<128>(d, ta, tb, args, tiles_upper, row_b, bf16, st);
+    p.tiles_upper = workspace ? p.d->num_sms
+                    : tiles > (int64_t(1) << 30) ? (1 << 30) : static_cast<int>(tiles);
+    p.row_b = bscale == FP8Q_BSCALE_ROW1x128;
+    p.bf16 = out_dtype == FP8Q_BF16;
+    return FP8Q_OK;
+}
+
+int gemm_launch(const GemmPlan& p, cudaStream_t st) {
+    return p.BN == 256
+               ? launch_gemm_bn<256>(p.d, p.ta, p.tb, p.args, p.tiles_upper, p.row_b, p.bf16, st)
+               : launch_gemm_bn<128>(p.d, p.ta, p.tb, p.args, p.tiles_upper, p.row_b, p.bf16, st);
+}
+
+int gemm_common(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB, void* C,
+                const int* m_offsets, int G, int64_t M, int64_t N, int64_t K, int out_dtype,
+                int bscale, void* workspace, size_t ws_bytes, cudaStream_t st) {
+    GemmPlan p;
+    const int rc = gemm_plan(A8, sA, B8, sB, C, m_offsets, G, M, N, K, out_dtype, bscale,
+                             workspace, ws_bytes, p);
+    return rc != FP8Q_OK ? rc : gemm_launch(p, st);
 }
 
 int check_in_dtype(int t) { return (t == FP8Q_F32 || t == FP8Q_BF16) ? FP8Q_OK : FP8Q_ERR_INVALID_ARG; }
@@ -440,30 +534,25 @@ int fp8q_gemm_grouped(const uint8_t* A8, const float* sA, const uint8_t* B8, con
 int fp8q_gemm_noalloc(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,
                       void* C, int64_t M, int64_t N, int64_t K, int out_dtype, int bscale,
                       fp8q_stream_t stream) {
-    // the same argument checks as the workspace GEMM, made before the counter
-    // clear below is launched (nothing is launched when they fail)
-    if (!A8 || !sA || !B8 || !sB || !C) return FP8Q_ERR_INVALID_ARG;
-    if (out_dtype != FP8Q_F32 && out_dtype != FP8Q_BF16) return FP8Q_ERR_INVALID_ARG;
-    if (bscale != FP8Q_BSCALE_BLOCK128 && bscale != FP8Q_BSCALE_ROW1x128) return FP8Q_ERR_INVALID_ARG;
-    if (M <= 0 || N <= 0 || K <= 0) return FP8Q_ERR_INVALID_ARG;
-    if (M % 128 || N % 128 || K % 128) return FP8Q_ERR_UNSUPPORTED_SHAPE;
-    if (M > (int64_t(1) << 30) || N > (int64_t(1) << 24) || K > (int64_t(1) << 30))
-        return FP8Q_ERR_UNSUPPORTED_SHAPE;
-    if (!aligned(A8, 16) || !aligned(B8, 16) || !aligned(sA, 16) || !aligned(C, 16))
-        return FP8Q_ERR_MISALIGNED;
-    if (!aligned(sB, bscale == FP8Q_BSCALE_ROW1x128 ? 16 : 4)) return FP8Q_ERR_MISALIGNED;
-    DeviceState* d = nullptr;
-    int rc = device_state(&d);
+    // Every check the workspace GEMM makes (arguments, shape limits, the TMA
+    // descriptors) is made before the counter clear below is queued, so that
+    // nothing is launched when one of them fails.
+    int rc = gemm_check_args(A8, sA, B8, sB, C, 1, M, N, K, out_dtype, bscale);
     if (rc != FP8Q_OK) return rc;
+    DeviceState* d = nullptr;
+    if ((rc = device_state(&d)) != FP8Q_OK) return rc;
     const size_t counters = kWsCounterBytes(d->num_sms);
     const size_t need = counters + kWsPartialBytes(d->num_sms);
     if (need > kNoAllocScratchBytes) return FP8Q_ERR_UNSUPPORTED_SHAPE;   // more SMs than it fits
+    GemmPlan p;
+    if ((rc = gemm_plan(A8, sA, B8, sB, C, nullptr, 1, M, N, K, out_dtype, bscale,
+                        d->noalloc_scratch, kNoAllocScratchBytes, p)) != FP8Q_OK)
+        return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // the arrival counters must start at zero; a call that failed on the
     // device may have left some set, so clear them every time
     if (cudaMemsetAsync(d->noalloc_scratch, 0, counters, st) != cudaSuccess) return cuda_fail();
-    return gemm_common(A8, sA, B8, sB, C, nullptr, 1, M, N, K, out_dtype, bscale,
-                       d->noalloc_scratch, kNoAllocScratchBytes, st);
+    return gemm_launch(p, st);
 }
 
 int fp8q_gemm_grouped_ws(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,
@@ -503,6 +592,27 @@ int fp8q_selftest_wait(int64_t limit_ns, fp8q_stream_t stream) {
     k_selftest_wait<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         d->status, static_cast<uint64_t>(limit_ns));
     return launched();
+}
+
+int fp8q_bench_mma_peak(int64_t blocks, fp8q_stream_t stream) {
+    if (blocks <= 0 || blocks > (int64_t(1) << 20)) return FP8Q_ERR_INVALID_ARG;
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != FP8Q_OK) return rc;
+    if (!d->peak_attr) {
+        if (cudaFuncSetAttribute(k_mma_peak, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPeakSmem) != cudaSuccess)
+            return cuda_fail();
+        d->peak_attr = true;
+    }
+    k_mma_peak<<<d->num_sms, 128, kPeakSmem, reinterpret_cast<cudaStream_t>(stream)>>>(
+        blocks, d->status);
+    return launched();
+}
+
+int fp8q_num_sms(void) {
+    DeviceState* d = nullptr;
+    return device_state(&d) == FP8Q_OK ? d->num_sms : -FP8Q_ERR_CUDA;
 }
 
 const char* fp8q_status_string(int status) {

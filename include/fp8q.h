@@ -275,6 +275,20 @@ FP8Q_API int fp8q_get_device_status(fp8q_stream_t stream);
  * of range.  Not part of the method; used by the library's tests. */
 FP8Q_API int fp8q_selftest_wait(int64_t limit_ns, fp8q_stream_t stream);
 
+/* Tensor-pipe throughput probe, a measurement aid (no counterpart on the
+ * pages): one CTA per SM issues `blocks` x 4 back-to-back
+ * tcgen05.mma.kind::f8f6f4 of shape 128 x 256 x 32 (E4M3 in, FP32 out) from
+ * fixed shared-memory operands into TMEM, then waits for them.  The work is
+ * fp8q_num_sms() * blocks * 2 * 128 * 256 * 128 flops; timing the launch with
+ * CUDA events on `stream` gives the dense FP8 rate the GEMM's roofline is
+ * compared with.  1 <= blocks <= 2^20 (FP8Q_ERR_INVALID_ARG otherwise; at
+ * 2^20 the launch runs about a quarter of a second).
+ * Nothing is read or written in global memory. */
+FP8Q_API int fp8q_bench_mma_peak(int64_t blocks, fp8q_stream_t stream);
+
+/* Number of SMs of the current device (negative fp8q_status on error). */
+FP8Q_API int fp8q_num_sms(void);
+
 /* Static, human-readable name of a status code. */
 FP8Q_API const char* fp8q_status_string(int status);
 

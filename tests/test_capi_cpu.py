@@ -131,6 +131,19 @@ def test_workspace_and_noalloc_argument_checks(lib):
     assert gw(*ok, None, 4, 512, 128, 128, 1, A16, 1 << 30, None) == 1
 
 
+def test_noalloc_checks_every_limit_before_launching(lib):
+    """fp8q_gemm_noalloc clears its counters with an asynchronous memset before
+    the GEMM; every shape limit of the workspace GEMM must be checked before
+    that.  2^30 x 2^24 passes the per-dimension limits but has 2^40 output
+    tiles: the call must answer FP8Q_ERR_UNSUPPORTED_SHAPE before it looks for
+    a device (without a GPU, reaching the device set-up answers
+    FP8Q_ERR_CUDA instead).  The pointers are fake and never dereferenced."""
+    ok = (A16, A16b, A16c, P(0x40000), P(0x50000))
+    na = lib.fp8q_gemm_noalloc
+    assert na(*ok, 1 << 30, 1 << 24, 128, 0, 0, None) == 2
+    assert na(*ok, 1 << 30, 1 << 24, 128, 1, 1, None) == 2
+
+
 def test_selftest_wait_limit_checks(lib):
     assert lib.fp8q_selftest_wait(0, None) == 1
     assert lib.fp8q_selftest_wait(-5, None) == 1
@@ -145,3 +158,54 @@ def test_python_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(128, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         fq.quant_act_1x128(x)
+
+
+def test_python_binding_checks_buffer_sizes(lib):
+    """The binding checks every buffer's size against the shapes it passes to
+    the library (which trusts them), before any device pointer is taken."""
+    import torch
+
+    import fp8_fine_grained_21_b300 as fq
+
+    u8, f32 = torch.uint8, torch.float32
+    M, N, K = 256, 384, 512
+    A8, B8 = torch.zeros(M, K, dtype=u8), torch.zeros(N, K, dtype=u8)
+    sA, sB = torch.zeros(K // 128, M, dtype=f32), torch.zeros(N // 128, K // 128, dtype=f32)
+    C = torch.zeros(M, N, dtype=f32)
+    for bad, what in (
+        (dict(C=torch.zeros(M, N + 128, dtype=f32)), "C must have shape"),
+        (dict(C=torch.zeros(M - 128, N, dtype=f32)), "C must have shape"),
+        (dict(B8=torch.zeros(N, K + 128, dtype=u8)), "same K"),
+        (dict(sA=torch.zeros(K // 128 - 1, M, dtype=f32)), "sA must hold"),
+        (dict(sB=torch.zeros(N // 128, K // 128 - 1, dtype=f32)), "sB must hold"),
+    ):
+        args = dict(A8=A8, sA=sA, B8=B8, sB=sB, C=C)
+        args.update(bad)
+        for fn in (fq.fp8q_gemm, fq.fp8q_gemm_ex, fq.fp8q_gemm_ws, fq.fp8q_gemm_noalloc):
+            with pytest.raises(ValueError, match=what):
+                fn(args["A8"], args["sA"], args["B8"], args["sB"], args["C"])
+    # 1x128 B scales are [K/128][N]: the block-scale count is refused
+    with pytest.raises(ValueError, match="sB must hold"):
+        fq.fp8q_gemm_ex(A8, sA, B8, sB, C, fq.BSCALE_ROW1x128)
+    # grouped: B8 [G][N][K], sB [G][N/128][K/128], m_offsets G + 1 entries
+    G = 3
+    Bg = torch.zeros(G, N, K, dtype=u8)
+    sBg = torch.zeros(G, N // 128, K // 128, dtype=f32)
+    offs = torch.zeros(G + 1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="sB must hold"):
+        fq.fp8q_gemm_grouped(A8, sA, Bg, sB, C, offs)
+    with pytest.raises(ValueError, match="m_offsets must hold"):
+        fq.fp8q_gemm_grouped_ws(A8, sA, Bg, sBg, C, offs[:G])
+    # quantizer outputs
+    x = torch.zeros(M, K, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="q must have shape"):
+        fq.fp8q_quant_act_1x128(x, torch.zeros(M, K - 16, dtype=u8), sA)
+    with pytest.raises(ValueError, match="s must hold"):
+        fq.fp8q_quant_act_1x128(x, A8, torch.zeros(K // 128, M - 1, dtype=f32))
+    with pytest.raises(ValueError, match="qT must have shape"):
+        fq.fp8q_quant_act_128x1(x, A8, torch.zeros(M // 128, K, dtype=f32))
+    with pytest.raises(ValueError, match="s must hold"):
+        fq.fp8q_quant_w_128x128(x, A8, torch.zeros(M // 128, K // 128 + 1, dtype=f32))
+    with pytest.raises(ValueError, match="q must have shape"):
+        fq.fp8q_rmsnorm_quant_1x128(x, torch.zeros(K, dtype=torch.bfloat16),
+                                    torch.zeros(M + 128, K, dtype=u8), sA)
