@@ -65,3 +65,42 @@ def test_two_percent_at_k4096_loose_pin(oracle):
     promoted = oracle.gemm_trunc_emu(A8, sA, B8, sB, kmax=4096, chunk=4, mbits=13, promote=128)
     rel_p = np.max(np.abs(promoted - ref) / np.abs(ref))
     assert rel_p < rel / 20, (rel_p, rel)
+
+
+def test_prefix_sum_pins(oracle):
+    """The FP64 prefix GEMM (the reference of the emulator's error) over the
+    first kmax < K elements: (1) a closed form whose two 128-element scale
+    groups carry different values, cut inside the second group, so that a
+    wrong group index or a wrong cut shows; (2) the independent exact int64
+    route applied to the K-truncated operands, for both B-scale layouts, at
+    the K = 4096 prefix of a K = 16384 problem (the accumulation-stress
+    shape's prefix)."""
+    # (1) A = 7 in group 0 and 14 in group 1, B = 7/16: the scales 2^-6, 2^-5 and
+    # 2^-10 are exact, every byte is 448, so every product and sum is exact
+    K = 256
+    A = np.concatenate([np.full((1, 128), 7.0), np.full((1, 128), 14.0)], axis=1).astype(np.float32)
+    B = np.full((1, K), 0.4375, np.float32)
+    A8, sA = oracle.quant_1x128(A)
+    B8, sB = oracle.quant_1x128(B)
+    for kmax, want in ((200, 128 * 7 * 0.4375 + 72 * 14 * 0.4375), (128, 392.0), (1, 3.0625),
+                       (256, 1176.0)):
+        got = oracle.gemm_prefix(A8, sA, B8, sB, kmax, bmode=1)[0, 0]
+        assert got == want, (kmax, got, want)
+    # (2) K-truncated operands through the exact integer route
+    M, N, K, kmax = 8, 128, 16384, 4096
+    A = fi.uniform((M, K), fi.rng_for(3, 0), 0.0, 1.0, bf16=False)
+    B = fi.uniform((N, K), fi.rng_for(3, 1), 0.0, 1.0, bf16=False)
+    A8, sA = oracle.quant_1x128(A)
+    kb = kmax // 128
+    for bmode in (0, 1):
+        B8, sB = oracle.quant_128x128(B) if bmode == 0 else oracle.quant_1x128(B)
+        ref = oracle.gemm_prefix(A8, sA, B8, sB, kmax, bmode=bmode)
+        sBt = sB[:, :kb] if bmode == 0 else sB[:kb]
+        cut = oracle.gemm_exact_int(np.ascontiguousarray(A8[:, :kmax]), np.ascontiguousarray(sA[:kb]),
+                                    np.ascontiguousarray(B8[:, :kmax]), np.ascontiguousarray(sBt),
+                                    bmode=bmode)
+        assert np.max(np.abs(ref - cut) / np.abs(cut)) <= 1e-13
+        # and the full-K prefix is the full GEMM
+        full = oracle.gemm_exact_int(A8, sA, B8, sB, bmode=bmode)
+        assert np.max(np.abs(oracle.gemm_prefix(A8, sA, B8, sB, K, bmode=bmode) - full)
+                      / np.abs(full)) <= 1e-13
