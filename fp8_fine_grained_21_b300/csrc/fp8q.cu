@@ -177,6 +177,22 @@ int encode_kmajor(CUtensorMap* map, const uint8_t* base, int64_t K, int64_t rows
     return r == CUDA_SUCCESS ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
+// Output C [rows][cols] (FP32 or BF16) for the GEMM epilogue's TMA stores:
+// boxes of 32 rows x 128 bytes with the 128-byte swizzle.
+int encode_out(CUtensorMap* map, void* base, int out_dtype, int64_t cols, int64_t rows) {
+    const bool bf = out_dtype == FP8Q_BF16;
+    const cuuint64_t es = bf ? 2 : 4;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * es};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), 32u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = g_encode(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                                2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
 // 2-D tensor [rows][cols] of FP32 or BF16 elements, row-major, boxes of
 // box_cols x box_rows copied unswizzled (a box lands in shared memory as
 // box_rows rows of box_cols elements); rows past the end read as zeros.
@@ -236,7 +252,7 @@ template <typename T> struct KQw { static constexpr auto fn = k_quant_128x128<T>
 
 template <int BN, bool kRowB, bool kBf16>
 int launch_gemm_inst(DeviceState* d, const CUtensorMap& ta, const CUtensorMap& tb,
-                     const GemmArgs& args, int tiles_upper, cudaStream_t st) {
+                     const CUtensorMap& tc, const GemmArgs& args, int tiles_upper, cudaStream_t st) {
     using S = GemmShape<BN>;
     auto kern = k_gemm<BN, kRowB, kBf16>;
     bool& attr = d->gemm_attr[BN == 256][kRowB][kBf16];
@@ -248,18 +264,19 @@ int launch_gemm_inst(DeviceState* d, const CUtensorMap& ta, const CUtensorMap& t
     }
     int grid = tiles_upper < d->num_sms ? tiles_upper : d->num_sms;
     if (grid < 1) grid = 1;
-    kern<<<grid, S::kThreads, S::kSmemBytes, st>>>(ta, tb, args);
+    kern<<<grid, S::kThreads, S::kSmemBytes, st>>>(ta, tb, tc, args);
     return cudaGetLastError() == cudaSuccess ? FP8Q_OK : cuda_fail();
 }
 
 template <int BN>
 int launch_gemm_bn(DeviceState* d, const CUtensorMap& ta, const CUtensorMap& tb,
-                   const GemmArgs& args, int tiles_upper, bool row_b, bool bf16, cudaStream_t st) {
+                   const CUtensorMap& tc, const GemmArgs& args, int tiles_upper, bool row_b,
+                   bool bf16, cudaStream_t st) {
     if (row_b)
-        return bf16 ? launch_gemm_inst<BN, true, true>(d, ta, tb, args, tiles_upper, st)
-                    : launch_gemm_inst<BN, true, false>(d, ta, tb, args, tiles_upper, st);
-    return bf16 ? launch_gemm_inst<BN, false, true>(d, ta, tb, args, tiles_upper, st)
-                : launch_gemm_inst<BN, false, false>(d, ta, tb, args, tiles_upper, st);
+        return bf16 ? launch_gemm_inst<BN, true, true>(d, ta, tb, tc, args, tiles_upper, st)
+                    : launch_gemm_inst<BN, true, false>(d, ta, tb, tc, args, tiles_upper, st);
+    return bf16 ? launch_gemm_inst<BN, false, true>(d, ta, tb, tc, args, tiles_upper, st)
+                : launch_gemm_inst<BN, false, false>(d, ta, tb, tc, args, tiles_upper, st);
 }
 
 // Stream-K workspace: arrival counters (one per promotion warp of each
@@ -276,7 +293,7 @@ constexpr size_t kWsPartialBytes(int sms) {
 // passed; gemm_launch then only launches.
 struct GemmPlan {
     DeviceState* d = nullptr;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, tc;
     GemmArgs args;
     int BN = 256;
     int tiles_upper = 1;
@@ -317,8 +334,10 @@ int gemm_plan(const uint8_t* A8, const float* sA, const uint8_t* B8, const float
     p.BN = (N % 256 == 0) ? 256 : 128;
     std::memset(&p.ta, 0, sizeof(p.ta));
     std::memset(&p.tb, 0, sizeof(p.tb));
+    std::memset(&p.tc, 0, sizeof(p.tc));
     if ((rc = encode_kmajor(&p.ta, A8, K, M, 128)) != FP8Q_OK) return rc;
     if ((rc = encode_kmajor(&p.tb, B8, K, int64_t(G) * N, p.BN)) != FP8Q_OK) return rc;
+    if ((rc = encode_out(&p.tc, C, out_dtype, N, M)) != FP8Q_OK) return rc;
     GemmArgs& a = p.args;
     a.sA = sA;
     a.sB = sB;
@@ -343,9 +362,10 @@ int gemm_plan(const uint8_t* A8, const float* sA, const uint8_t* B8, const float
 }
 
 int gemm_launch(const GemmPlan& p, cudaStream_t st) {
-    return p.BN == 256
-               ? launch_gemm_bn<256>(p.d, p.ta, p.tb, p.args, p.tiles_upper, p.row_b, p.bf16, st)
-               : launch_gemm_bn<128>(p.d, p.ta, p.tb, p.args, p.tiles_upper, p.row_b, p.bf16, st);
+    return p.BN == 256 ? launch_gemm_bn<256>(p.d, p.ta, p.tb, p.tc, p.args, p.tiles_upper,
+                                             p.row_b, p.bf16, st)
+                       : launch_gemm_bn<128>(p.d, p.ta, p.tb, p.tc, p.args, p.tiles_upper,
+                                             p.row_b, p.bf16, st);
 }
 
 int gemm_common(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB, void* C,

@@ -64,17 +64,23 @@ struct GemmShape {
     static_assert(!kRealloc || 128 * kCtrlRegs + 128 * kHalves * kPromoRegs <= kThreads * 168,
                   "register split exceeds the launch allocation");
     static_assert(kMmaWarp > 0 && kMmaWarp < 4, "MMA warp must be a control warp");
-    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr int kStages = BN == 256 ? 3 : 5;
     static constexpr int kABytes = kBM * kBK;
     static constexpr int kBBytes = BN * kBK;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kTbufs = 512 / BN;              // TMEM partial buffers in flight
+    static constexpr int kTmemCols = kTbufs * BN;
+    // epilogue staging: per promotion warp, two 32-row x 128-byte boxes of C
+    // laid out with the 128-byte swizzle the C tensor map uses
+    static constexpr int kEpiBoxBytes = 32 * 128;
+    static constexpr int kEpiWarpBytes = 2 * kEpiBoxBytes;
+    static constexpr int kOffEpi = kStages * kStageBytes;
     static constexpr int kSaBytes = kBM * 4;
     static constexpr int kSbBytes = BN * 4;
     static constexpr int kSlotBytes = kSaBytes + kSbBytes;
-    static constexpr int kOffScale = kStages * kStageBytes;
+    static constexpr int kOffScale = kOffEpi + kPromoWarps * kEpiWarpBytes;
     static constexpr int kOffBars = kOffScale + kScaleSlots * kSlotBytes;
-    static constexpr int kNumBars = 2 * kStages + 2 * kScaleSlots + 5;
+    static constexpr int kNumBars = 2 * kStages + 2 * kScaleSlots + 2 * kTbufs + 1;
     static constexpr int kOffMisc = kOffBars + kNumBars * 8;
     static constexpr int kOffSched = kOffMisc + 32;
     static constexpr int kOffGroups = kOffSched + 64;
@@ -242,10 +248,58 @@ __device__ __forceinline__ TileCoord decode_tile(int t, bool grouped, int N, int
     return tc;
 }
 
+// One promotion warp's epilogue: its 32 rows x 128 columns of C, held as one
+// row per thread in acc, go out through shared memory and TMA stores.  Each
+// round stages two boxes of 32 rows x 128 bytes (64 BF16 or 32 FP32 columns)
+// in the warp's own staging area, 16-byte chunk j of row r at chunk position
+// j ^ (r % 8) (the 128-byte swizzle, which also spreads the lanes' stores
+// over all shared-memory banks), then lane 0 issues the two box stores.
+// BF16 output takes one round, FP32 two; before a round overwrites the
+// staging area, lane 0 waits until the previous stores have read it.
+template <bool kBf16Out>
+__device__ __forceinline__ void store_tile_tma(const float2* acc, uint8_t* stg,
+                                               const CUtensorMap* tmC, int x0, int y0, int lane) {
+    constexpr int kColsPerBox = kBf16Out ? 64 : 32;
+    constexpr int kRounds = kBf16Out ? 1 : 2;
+#pragma unroll
+    for (int rd = 0; rd < kRounds; ++rd) {
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int bx = 0; bx < 2; ++bx) {
+            const int box = rd * 2 + bx;
+            uint8_t* row = stg + bx * 4096 + lane * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint4 v;
+                if (kBf16Out) {
+                    const float2* a = acc + box * 32 + j * 4;
+                    v.x = pack_bf16x2(a[0].x, a[0].y);
+                    v.y = pack_bf16x2(a[1].x, a[1].y);
+                    v.z = pack_bf16x2(a[2].x, a[2].y);
+                    v.w = pack_bf16x2(a[3].x, a[3].y);
+                } else {
+                    const float2* a = acc + box * 16 + j * 2;
+                    v = make_uint4(__float_as_uint(a[0].x), __float_as_uint(a[0].y),
+                                   __float_as_uint(a[1].x), __float_as_uint(a[1].y));
+                }
+                *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = v;
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmC, stg, x0 + (rd * 2) * kColsPerBox, y0);
+            tma_store_2d(tmC, stg + 4096, x0 + (rd * 2 + 1) * kColsPerBox, y0);
+            bulk_commit_group();
+        }
+    }
+}
+
 template <int BN, bool kRowB, bool kBf16Out>
 __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-           const GemmArgs args) {
+           const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
     using S = GemmShape<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -256,8 +310,8 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
     uint64_t* sfull = empty + S::kStages;
     uint64_t* sempty = sfull + kScaleSlots;
     uint64_t* tfull = sempty + kScaleSlots;
-    uint64_t* tempty = tfull + 2;
-    uint64_t* drain = tempty + 2;
+    uint64_t* tempty = tfull + S::kTbufs;
+    uint64_t* drain = tempty + S::kTbufs;
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + S::kOffMisc);
     Sched* sched_smem = reinterpret_cast<Sched*>(smem + S::kOffSched);
     int* gtile = reinterpret_cast<int*>(smem + S::kOffGroups);
@@ -278,10 +332,11 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
             mbar_init(&sfull[i], 1);
             mbar_init(&sempty[i], S::kPromoWarps);
         }
-        mbar_init(&tfull[0], 1);
-        mbar_init(&tfull[1], 1);
-        mbar_init(&tempty[0], S::kPromoWarps);
-        mbar_init(&tempty[1], S::kPromoWarps);
+#pragma unroll 1
+        for (int i = 0; i < S::kTbufs; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], S::kPromoWarps);
+        }
         mbar_init(drain, 1);
         fence_mbar_init();
         int bad = 0, tiles = 0;
@@ -314,6 +369,7 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
     if (warp == S::kProducerWarp && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmC);
     }
     tc_fence_before();
     __syncthreads();
@@ -346,6 +402,7 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
                         // weight-gradient form: both operands' 1x128 scales of
                         // this block go through a shared-memory slot
                         if (!mbar_wait(&sempty[slot], sphase ^ 1, args.status)) { ok = false; break; }
+                        fence_proxy_async_smem();
                         float* sl = reinterpret_cast<float*>(smem + S::kOffScale + slot * S::kSlotBytes);
                         mbar_arrive_expect_tx(&sfull[slot], S::kSlotBytes);
                         bulk_load(sl, args.sA + static_cast<size_t>(kb) * args.M_total + tc.arow,
@@ -368,7 +425,7 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
             while (ok && si.next(sg)) {
 #pragma unroll 1
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
-                    const uint32_t b = it & 1, tph = (it >> 1) & 1;
+                    const uint32_t b = it % S::kTbufs, tph = (it / S::kTbufs) & 1;
                     if (!mbar_wait(&tempty[b], tph ^ 1, args.status)) { ok = false; break; }
                     tc_fence_after();
                     if (!mbar_wait(&full[stage], phase, args.status)) { ok = false; break; }
@@ -431,7 +488,7 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
             for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
 #pragma unroll 1
             for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
-                const uint32_t b = it & 1, tph = (it >> 1) & 1;
+                const uint32_t b = it % S::kTbufs, tph = (it / S::kTbufs) & 1;
                 float fa, f;
                 const float* sbc = nullptr;
                 if (!kRowB) {
@@ -502,6 +559,11 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
                         promote_chunk<true>(acc + (c + 1) * 4, r1, f, fa, sbc + (c + 1) * 8);
                         if (c + 2 < 16) tmem_ld_wait(r0);
                     }
+                }
+                if (kRowB) {
+                    // the slot was read with generic loads and is refilled by the
+                    // async proxy (a bulk copy): order the reads before that write
+                    fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sempty[slot]);
                     if (++slot == kScaleSlots) { slot = 0; sphase ^= 1; }
@@ -558,27 +620,11 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
                 }
             }
             // ------------------------------------------------ epilogue
-            const size_t crow = static_cast<size_t>(tc.arow + row);
-            const int ccol = tc.n0 + half * 128;
-            if (kBf16Out) {
-                __nv_bfloat16* cp = reinterpret_cast<__nv_bfloat16*>(args.C) + crow * N + ccol;
-#pragma unroll
-                for (int j = 0; j < 64; j += 4) {
-                    uint4 v;
-                    v.x = pack_bf16x2(acc[j].x, acc[j].y);
-                    v.y = pack_bf16x2(acc[j + 1].x, acc[j + 1].y);
-                    v.z = pack_bf16x2(acc[j + 2].x, acc[j + 2].y);
-                    v.w = pack_bf16x2(acc[j + 3].x, acc[j + 3].y);
-                    *reinterpret_cast<uint4*>(cp + 2 * j) = v;
-                }
-            } else {
-                float* cp = reinterpret_cast<float*>(args.C) + crow * N + ccol;
-#pragma unroll
-                for (int j = 0; j < 64; j += 2)
-                    *reinterpret_cast<float4*>(cp + 2 * j) =
-                        make_float4(acc[j].x, acc[j].y, acc[j + 1].x, acc[j + 1].y);
-            }
+            store_tile_tma<kBf16Out>(acc, smem + S::kOffEpi + pw * S::kEpiWarpBytes, &tmC,
+                                     tc.n0 + half * 128, tc.arow + quarter * 32, lane);
         }
+        if (lane == 0) bulk_wait_all();       // this warp's C stores have landed
+        __syncwarp();
         tc_fence_before();
         cta_barrier(S::kThreads);
     }

@@ -86,3 +86,32 @@ def check_fused_1x128(oracle, q_gpu, s_gpu, h, q_o, s_o, h_rel, s_rel, what):
         what, len(bad), tuple(bad[0]), d[tuple(bad[0])], lo[tuple(bad[0])], hi[tuple(bad[0])])
     same = np.mean(np.asarray(q_gpu) == q_o)
     assert same >= 0.999, "%s: only %.4f of codes equal the oracle's" % (what, same)
+
+
+GUARD_BYTES = 4096          # guard band on each side (keeps 16-byte alignment)
+SENTINEL = 0xA7
+
+
+class Guarded:
+    """A CUDA output tensor of `shape` and `dtype` placed inside a larger byte
+    buffer whose guard bands, GUARD_BYTES before and after it, hold a sentinel
+    byte.  check() asserts that a kernel wrote nothing outside the tensor (the
+    stand-in for a memory checker on the GPU)."""
+
+    def __init__(self, shape, dtype, device="cuda", fill=None):
+        es = torch.empty((), dtype=dtype).element_size()
+        self.nbytes = int(np.prod(shape)) * es
+        self.buf = torch.full((2 * GUARD_BYTES + self.nbytes,), SENTINEL, dtype=torch.uint8,
+                              device=device)
+        self.t = self.buf[GUARD_BYTES:GUARD_BYTES + self.nbytes].view(dtype).view(tuple(shape))
+        if fill is not None:
+            self.t.fill_(fill)
+
+    def check(self, what=""):
+        torch.cuda.synchronize()
+        head = self.buf[:GUARD_BYTES]
+        tail = self.buf[GUARD_BYTES + self.nbytes:]
+        nh = int((head != SENTINEL).sum().item())
+        nt = int((tail != SENTINEL).sum().item())
+        assert nh == 0 and nt == 0, "%s: %d bytes written before and %d after the buffer" % (
+            what, nh, nt)

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import fp8q_inputs as fi
-from helpers import assert_gemm_close, cpu, to_dev
+from helpers import Guarded, assert_gemm_close, cpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -45,11 +45,14 @@ def sample_entries(M, N, BN, rng, extra=2048):
     return mi.astype(np.int64), ni.astype(np.int64)
 
 
-def run_gemm_only(fq, oracle, A, B, out_dtype, bmode=0, full=True, seed=0):
+def run_gemm_only(fq, oracle, A, B, out_dtype, bmode=0, full=True, seed=0, stream_k=True):
     A8, sA, B8, sB = oracle_operands(oracle, A, B, bmode)
-    C = fq.gemm(to_dev(A8), to_dev(sA), to_dev(B8), to_dev(sB), out_dtype=out_dtype, bscale=bmode)
+    Cgd = Guarded((A8.shape[0], B8.shape[0]), out_dtype, fill=float("nan"))
+    fq.fp8q_gemm_ws(to_dev(A8), to_dev(sA), to_dev(B8), to_dev(sB), Cgd.t, bmode,
+                    fq.workspace() if stream_k else None)
     assert fq.fp8q_get_device_status() == 0
-    Cg = cpu(C).astype(np.float64)
+    Cgd.check("C")
+    Cg = cpu(Cgd.t).astype(np.float64)
     bf16 = out_dtype == torch.bfloat16
     if full:
         Cref, Cabs = oracle.gemm(A8, sA, B8, sB, bmode=bmode)
@@ -72,6 +75,7 @@ def test_dense_small(fq, oracle, out, M, N, K):
     A = fi.gaussian((M, K), fi.rng_for(M + N, 0), 1.0, 0.001, 100.0, bf16=False)
     B = fi.gaussian((N, K), fi.rng_for(M + N, 1), 0.02, bf16=False)
     run_gemm_only(fq, oracle, A, B, out)
+    run_gemm_only(fq, oracle, A, B, out, stream_k=False)
 
 
 def test_dense_persistent_multi_tile(fq, oracle):
@@ -99,6 +103,57 @@ def test_dense_zero_and_constant(fq, oracle):
     Bc = np.full((N, K), -0.4375, np.float32)
     C = fq.gemm(*[to_dev(t) for t in oracle_operands(oracle, A, Bc)], out_dtype=torch.float32)
     assert torch.all(C == K * 7.0 * -0.4375).item()
+
+
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("stream_k", [False, True])
+def test_wgrad_row_scales_128_wide_tiles(fq, oracle, out, stream_k):
+    """Row-scaled B (the weight-gradient form) with N % 256 != 0 takes the
+    128-column tile instantiation, whose 1x128 B-scale slots and stream-K
+    fix-up slices differ from the 256-column one.  3 x 3 tiles of 40 K
+    blocks: with a workspace the stream-K schedule cuts every tile."""
+    M, N, K = 384, 384, 5120
+    dY = fi.gaussian((K, M), fi.rng_for(31, 0), 1.0, 0.001, 100.0, bf16=False)
+    X = fi.gaussian((K, N), fi.rng_for(31, 1), 1.0, 0.001, 100.0, bf16=False)
+    A8, sA = oracle.quant_128x1(dY)
+    B8, sB = oracle.quant_128x1(X)
+    Cgd = Guarded((M, N), out, fill=float("nan"))
+    fq.fp8q_gemm_ws(to_dev(A8), to_dev(sA), to_dev(B8), to_dev(sB), Cgd.t, fq.BSCALE_ROW1x128,
+                    fq.workspace() if stream_k else None)
+    assert fq.fp8q_get_device_status() == 0
+    Cgd.check("C")
+    Cref, Cabs = oracle.gemm(A8, sA, B8, sB, bmode=1)
+    assert_gemm_close(cpu(Cgd.t), Cref, Cabs, out == torch.bfloat16, "wgrad 128-wide tiles")
+
+
+@pytest.mark.parametrize("stream_k", [True, False])
+def test_wgrad_row_scales_scale_slot_reuse(fq, oracle, stream_k):
+    """With 128-column tiles the TMA producer can run more than eight K blocks
+    ahead of the promotion warps, so it waits on the ring of 1x128 scale
+    slots and refills a slot as soon as the last promotion warp releases it.
+    The slot is read with ordinary loads and refilled by a bulk copy, so the
+    release must order those reads before the copy's write; when it did not,
+    the slowest warp read some later B scales of the next block.  Several
+    whole 128 x 128 tiles are checked, and every tile's corners."""
+    T, M, N = 2048, 2048, 1152
+    dY = fi.gaussian((T, M), fi.rng_for(41, 0), 1.0, 0.001, 100.0, bf16=False)
+    X = fi.gaussian((T, N), fi.rng_for(41, 1), 1.0, 0.001, 100.0, bf16=False)
+    A8, sA = oracle.quant_128x1(dY)
+    B8, sB = oracle.quant_128x1(X)
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    fq.fp8q_gemm_ws(to_dev(A8), to_dev(sA), to_dev(B8), to_dev(sB), C, fq.BSCALE_ROW1x128,
+                    fq.workspace() if stream_k else None)
+    assert fq.fp8q_get_device_status() == 0
+    Cg = cpu(C).astype(np.float64)
+    for tm, tn in ((0, 0), (3, 5), (15, 8), (7, 2), (10, 7)):
+        r, c = slice(tm * 128, tm * 128 + 128), slice(tn * 128, tn * 128 + 128)
+        Cref, Cabs = oracle.gemm(A8[r], sA[:, r], B8[c], sB[:, c], bmode=1)
+        assert_gemm_close(Cg[r, c], Cref, Cabs, False, "tile (%d, %d)" % (tm, tn))
+    rows = np.concatenate([np.arange(0, M, 128), np.arange(127, M, 128)])
+    cols = np.concatenate([np.arange(0, N, 128), np.arange(127, N, 128)])
+    mi, ni = np.repeat(rows, len(cols)), np.tile(cols, len(rows))
+    Cref, Cabs = oracle.gemm_entries(A8, sA, B8, sB, mi, ni, bmode=1)
+    assert_gemm_close(Cg[mi, ni], Cref, Cabs, False, "tile corners")
 
 
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])

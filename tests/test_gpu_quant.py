@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import fp8q_inputs as fi
-from helpers import cpu, to_dev
+from helpers import Guarded, cpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -58,10 +58,13 @@ def special_tile_input(M, K, bf16, seed):
 @pytest.mark.parametrize("M,K", [(1, 128), (64, 256), (200, 384), (333, 1024)])
 def test_quant_1x128_small(fq, oracle, bf16, M, K):
     x = special_tile_input(M, K, bf16, seed=M + K)
-    q, s = fq.quant_act_1x128(to_dev(x))
+    q, s = Guarded((M, K), torch.uint8), Guarded((K // 128, M), torch.float32)
+    fq.fp8q_quant_act_1x128(to_dev(x), q.t, s.t)
+    q.check("q")
+    s.check("s")
     qo, so = oracle.quant_1x128(x)
-    assert_bytes_equal(cpu(q), qo, "q")
-    assert_scales_equal(cpu(s), so, "s")
+    assert_bytes_equal(cpu(q.t), qo, "q")
+    assert_scales_equal(cpu(s.t), so, "s")
 
 
 @pytest.mark.parametrize("bf16", [True, False])
@@ -75,20 +78,26 @@ def test_quant_128x1_small(fq, oracle, bf16, T, C):
     x[-1, 3] = -6.0                                 # one-hot in the last token group
     if bf16:
         x = fi.to_bf16_bits(x)
-    q, s = fq.quant_act_128x1(to_dev(x))
+    q, s = Guarded((C, T), torch.uint8), Guarded((T // 128, C), torch.float32)
+    fq.fp8q_quant_act_128x1(to_dev(x), q.t, s.t)
+    q.check("qT")
+    s.check("sT")
     qo, so = oracle.quant_128x1(x)
-    assert_bytes_equal(cpu(q), qo, "qT")
-    assert_scales_equal(cpu(s), so, "sT")
+    assert_bytes_equal(cpu(q.t), qo, "qT")
+    assert_scales_equal(cpu(s.t), so, "sT")
 
 
 @pytest.mark.parametrize("bf16", [True, False])
 @pytest.mark.parametrize("N,K", [(128, 128), (256, 384), (384, 1024)])
 def test_quant_128x128_small(fq, oracle, bf16, N, K):
     x = special_tile_input(N, K, bf16, seed=N * 5 + K)
-    q, s = fq.quant_w_128x128(to_dev(x))
+    q, s = Guarded((N, K), torch.uint8), Guarded((N // 128, K // 128), torch.float32)
+    fq.fp8q_quant_w_128x128(to_dev(x), q.t, s.t)
+    q.check("q")
+    s.check("s")
     qo, so = oracle.quant_128x128(x)
-    assert_bytes_equal(cpu(q), qo, "q")
-    assert_scales_equal(cpu(s), so, "s")
+    assert_bytes_equal(cpu(q.t), qo, "q")
+    assert_scales_equal(cpu(s.t), so, "s")
 
 
 def test_quant_tiny_workload_full(fq, oracle):
