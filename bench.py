@@ -3,9 +3,13 @@
 One step = one pass of the whole path over one batch of synthetic input:
 online quantization of the activations (1x128 tiles) and of the weights
 (128x128 blocks), then the block-scaled FP8 GEMM.  Default workload: the
-forward-shaped dense problem A[4096][7168] BF16 x W[2048][7168] BF16 -> C BF16.
-Other workloads (--workload wgrad | accum | grouped) use the same step
-structure with their own quantizers and GEMM form.
+grouped MoE problem (32 experts, 16384 tokens routed with Zipf 1.1, each
+expert's rows rounded up to 128, K = 7168, N = 2048, BF16 in and out), the
+largest configuration that fits one GPU.  The same JSON line also carries the
+weight-gradient GEMM dW[7168][2048] = dY^T X over T = 8192 (the largest dense
+shape) under "dense_headline".  Other workloads (--workload forward | wgrad |
+accum | backward | mlp_down | forward_norm) use the same step structure with
+their own quantizers and GEMM form.
 
 Prints ONE JSON line (rank 0).  `value` is whole-step throughput in TFLOPS
 (2*M*N*K of the GEMM per step, over the step's device time with inputs
@@ -383,6 +387,39 @@ def time_graph(g, n, stream, flush):
     return float(t.mean()), float(t.min())
 
 
+KERNEL_REPLAYS = 200             # per-kernel timing: replays, whatever --steps is
+
+
+def mma_peak(fq, stream, launches=40, blocks=8192):
+    """Dense FP8 tensor-pipe rate measured on this GPU: the library's
+    MMA-only probe (128 x 256 x 32 E4M3 MMAs back to back on every SM),
+    `launches` launches of `blocks` 128-K blocks per SM each, timed with CUDA
+    events; the SM clock is sampled meanwhile."""
+    sms = fq.fp8q_num_sms()
+    flops = sms * blocks * 2.0 * 128 * 256 * 128
+    fq.fp8q_bench_mma_peak(blocks, stream)          # warm-up
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    evs = []
+    for _ in range(launches):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fq.fp8q_bench_mma_peak(blocks, stream)
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    status = fq.fp8q_get_device_status()
+    if status != 0:
+        raise RuntimeError("MMA probe: %s" % fq.fp8q_status_string(status))
+    ms = float(np.median([a.elapsed_time(b) for a, b in evs]))
+    return {"tflops": flops / (ms * 1e-3) / 1e12, "ms_per_launch": ms, "sms": sms,
+            "probe": "tcgen05.mma.cta_group::1.kind::f8f6f4 128x256x32, %d per SM per launch, "
+                     "median of %d launches" % (4 * blocks, launches),
+            "clocks": clocks}
+
+
 def time_quant_back_to_back(wl, stream, flush, reps=20):
     """Per-launch time of each quantizer when launched back to back (one CUDA
     graph) over R distinct copies of its input, R chosen so that the copies
@@ -437,6 +474,33 @@ def time_e2e(wl, steps, stream):
     h2d = sum(h.numel() * h.element_size() for h in hin)
     d2h = hout.numel() * hout.element_size()
     return {"ms": max(wall, dev), "h2d": h2d, "d2h": d2h}
+
+
+def dense_headline(fq, device, stream, flush):
+    """The weight-gradient workload (the largest dense shape) timed beside the
+    default grouped one: its step, its GEMM and its two quantizers, each
+    kernel over KERNEL_REPLAYS replays with the same flush discipline."""
+    wl = Workload("wgrad", seed=0, device=device)
+    g_step = capture(wl.step)
+    g_parts = [capture(wl.quant0), capture(wl.quant1), capture(wl.gemm)]
+    for _ in range(3):
+        flush()
+        g_step.replay()
+    torch.cuda.synchronize()
+    step_ms, _ = time_graph(g_step, 50, stream, flush)
+    kt = [time_graph(g, KERNEL_REPLAYS, stream, flush) for g in g_parts]
+    status = fq.fp8q_get_device_status()
+    if status != 0:
+        raise RuntimeError("device status after the dense headline: %s" % fq.fp8q_status_string(status))
+    gemm_tflops = wl.flops / (kt[2][0] * 1e-3) / 1e12
+    out = {"workload": wl.desc, "M": wl.M, "N": wl.N, "K": wl.K, "step_ms": step_ms,
+           "step_tflops": wl.flops / (step_ms * 1e-3) / 1e12, "gemm_tflops": gemm_tflops,
+           "gemm_ms": kt[2][0], "quant_ms": [kt[0][0], kt[1][0]],
+           "quant_gbs": [wl.quant_bytes[i] / (kt[i][0] * 1e-3) / 1e9 for i in range(2)],
+           "gemm_traffic": profiled_traffic("gemm_wgrad")}
+    del g_step, g_parts, wl
+    torch.cuda.synchronize()
+    return out
 
 
 # --------------------------------------------------------------- CPU oracle
@@ -585,13 +649,16 @@ def run_fp8q(args):
         dist.barrier()
     wall_ms = (time.perf_counter() - t_wall0) * 1e3
     # per-kernel device times (same flush discipline), for the roofline line
-    nk = max(10, min(args.steps, 100))
-    kt = [time_graph(g, nk, stream, flush) for g in g_parts]
+    kt = [time_graph(g, KERNEL_REPLAYS, stream, flush) for g in g_parts]
     q_b2b = time_quant_back_to_back(wl, stream, flush)
     clocks = sampler.stop()
     status = fq.fp8q_get_device_status()
     if status != 0:
         raise RuntimeError("device status after timing: %s" % fq.fp8q_status_string(status))
+    dense = None
+    if args.workload == "grouped" and not args.no_dense_headline:
+        dense = dense_headline(fq, device, stream, flush)
+    peak_probe = mma_peak(fq, stream) if not args.no_mma_peak else None
 
     step_ms = max_over_ranks(step_ms, dist, device)
     e2e = time_e2e(wl, max(3, min(args.steps, 20)), stream) if not args.no_e2e else None
@@ -604,6 +671,7 @@ def run_fp8q(args):
 
     peaks = measured_peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops"]          # FP8 dense = 2 x BF16 dense (nominal ratio)
+    mma_meas = peak_probe["tflops"] if peak_probe else None
     gemm_ms = kt[2][0]
     gemm_tflops = wl.flops / (gemm_ms * 1e-3) / 1e12
     value = job_tflops(world, wl.flops, step_ms)
@@ -633,17 +701,25 @@ def run_fp8q(args):
             "frac_of_hbm": wl.quant_bytes[i] / (b["ms_per_launch"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
             for i, b in enumerate(q_b2b)],
         "kernel_ms": {"quant_a": kt[0][0], "quant_b": kt[1][0], "gemm": gemm_ms,
-                      "gemm_min": kt[2][1]},
+                      "gemm_min": kt[2][1], "replays": KERNEL_REPLAYS},
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
                      "traffic": profiled_traffic("gemm_" + args.workload),
                      "kernel": "k_gemm",
                      "peak_source": "2 x bf16 burst (%s)" % peaks["source"],
-                     "algorithmic_bytes": wl.gemm_bytes},
+                     "algorithmic_bytes": wl.gemm_bytes,
+                     "frac_of_mma_peak_measured": gemm_tflops / mma_meas if mma_meas else None},
+        "fp8_mma_peak_measured": peak_probe,
         "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": clocks,
         "wall_ms_timed_region": wall_ms,
     }
+    if dense:
+        dense["gemm_frac_of_fp8_peak"] = dense["gemm_tflops"] / fp8_peak
+        dense["gemm_frac_of_mma_peak_measured"] = (dense["gemm_tflops"] / mma_meas
+                                                   if mma_meas else None)
+        dense["quant_frac_of_hbm"] = [q / peaks["hbm_gbs"] for q in dense["quant_gbs"]]
+        out["dense_headline"] = dense
     if e2e:
         out["e2e"] = {"value": job_tflops(world, wl.flops, e2e_ms), "unit": "TFLOPS",
                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
@@ -671,8 +747,12 @@ def main():
     ap.add_argument("--impl", choices=["fp8q", "reference"], default="fp8q")
     ap.add_argument("--workload", choices=["forward", "wgrad", "accum", "grouped", "backward",
                                            "mlp_down", "forward_norm"],
-                    default="forward")
+                    default="grouped")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-dense-headline", action="store_true",
+                    help="skip the weight-gradient figures added to the grouped workload's line")
+    ap.add_argument("--no-mma-peak", action="store_true",
+                    help="skip the tensor-pipe probe")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "fp8q" and args.warmup < 3:
