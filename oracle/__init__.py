@@ -306,3 +306,49 @@ def gemm_prefix(A8, sA, B8, sB, kmax, bmode=BSCALE_BLOCK128, threads=0):
     _load().fpo_gemm_f64_prefix(_ptr(A8), _ptr(sA), _ptr(B8), _ptr(sB), bmode, M, N, K,
                                 int(kmax), _ptr(C), threads)
     return C
+
+
+# ------------------------------------------------------ expert-parallel MoE
+def bf16_round(x):
+    """FP64 -> nearest BF16 value (as FP64), ties to even: the rounding of a
+    BF16 output.  Plain definition: x = m 2^e with 1/2 <= |m| < 1 (frexp,
+    exact); BF16 keeps 8 significant bits, so the result is rint(256 m) 2^(e-8)
+    with numpy's rint rounding halves to even (a carry to 256 lands on the
+    next power of two, which is representable).  Finite, normal-range values."""
+    x = np.asarray(x, np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def moe_ep_reference(x, topk_ids, topk_w, W8, sW):
+    """Expert-parallel MoE layer with FP8 dispatch and BF16 combine ("Six
+    Reasons Deepseek Ai Is A Waste Of Time", para. 4: the activations are
+    quantized to FP8 before they are dispatched to the experts' up
+    projection, and the combine stays in BF16).  Token t's activations are
+    quantized per 1x128 tile; for each of its k experts e = topk_ids[t][j] the
+    expert's block-scaled FP8 GEMM gives y_tj = dequant(q_t) . dequant(W8_e)^T
+    (FP64 here), returned as BF16; the output is
+        out[t] = bf16( sum_j topk_w[t][j] * bf16(y_tj) ).
+      x        [T][H] activations (BF16 bits as uint16, or FP32)
+      topk_ids [T][k] expert ids in [0, E), distinct within a row
+      topk_w   [T][k] gate weights (FP32)
+      W8, sW   [E][N][H] uint8, [E][N/128][H/128] float32: the experts'
+               weights quantized per 128x128 block
+    Returns (out [T][N], y [T][k][N] exact expert results, yabs [T][k][N]
+    sum_h |a_h b_h|), all FP64; out holds BF16 values."""
+    q, s = quant_1x128(x)
+    ids = np.asarray(topk_ids, np.int64)
+    w = np.asarray(topk_w, np.float32).astype(np.float64)
+    T, k = ids.shape
+    E, N, H = W8.shape
+    y = np.zeros((T, k, N))
+    yabs = np.zeros((T, k, N))
+    for e in range(E):
+        ts, js = np.nonzero(ids == e)
+        if ts.size == 0:
+            continue
+        Ce, Ca = gemm(q[ts], s[:, ts], W8[e], sW[e])
+        y[ts, js] = Ce
+        yabs[ts, js] = Ca
+    out = bf16_round(np.einsum("tk,tkn->tn", w, bf16_round(y)))
+    return out, y, yabs
