@@ -19,7 +19,9 @@ __all__ = [
     "fp8q_retile_1x128_to_128x1", "fp8q_transpose_w_128x128", "retile_1x128_to_128x1",
     "transpose_w_128x128",
     "fp8q_gemm", "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_gemm_ws", "fp8q_gemm_grouped_ws",
-    "fp8q_gemm_workspace_size", "fp8q_gemm_noalloc", "fp8q_get_device_status",
+    "fp8q_gemm_workspace_size", "fp8q_gemm_noalloc", "fp8q_gemm_quant_a", "gemm_quant_a",
+    "fp8q_ep_row_bytes", "fp8q_ep_route", "fp8q_ep_pack", "fp8q_ep_unpack", "fp8q_ep_gather",
+    "fp8q_ep_combine", "fp8q_get_device_status",
     "fp8q_selftest_wait", "fp8q_bench_mma_peak", "fp8q_num_sms", "fp8q_status_string",
     "fp8q_version", "workspace",
     "quant_act_1x128", "quant_act_128x1", "quant_w_128x128", "gemm", "gemm_grouped",
@@ -33,12 +35,14 @@ F32, BF16 = 0, 1
 BSCALE_BLOCK128, BSCALE_ROW1x128 = 0, 1
 STATUS_NAMES = {0: "FP8Q_OK", 1: "FP8Q_ERR_INVALID_ARG", 2: "FP8Q_ERR_UNSUPPORTED_SHAPE",
                 3: "FP8Q_ERR_MISALIGNED", 4: "FP8Q_ERR_CUDA", 5: "FP8Q_ERR_TIMEOUT",
-                6: "FP8Q_ERR_BAD_GROUPS"}
+                6: "FP8Q_ERR_BAD_GROUPS", 7: "FP8Q_ERR_BAD_ROUTING"}
 EXPORTS = ("fp8q_quant_act_1x128", "fp8q_quant_act_128x1", "fp8q_quant_w_128x128",
            "fp8q_swiglu_quant_1x128", "fp8q_rmsnorm_quant_1x128",
            "fp8q_retile_1x128_to_128x1", "fp8q_transpose_w_128x128", "fp8q_gemm",
            "fp8q_gemm_ex", "fp8q_gemm_grouped", "fp8q_gemm_ws", "fp8q_gemm_grouped_ws",
-           "fp8q_gemm_workspace_size", "fp8q_gemm_noalloc", "fp8q_get_device_status",
+           "fp8q_gemm_workspace_size", "fp8q_gemm_noalloc", "fp8q_gemm_quant_a",
+           "fp8q_ep_row_bytes", "fp8q_ep_route", "fp8q_ep_pack", "fp8q_ep_unpack",
+           "fp8q_ep_gather", "fp8q_ep_combine", "fp8q_get_device_status",
            "fp8q_selftest_wait", "fp8q_bench_mma_peak", "fp8q_num_sms", "fp8q_status_string",
            "fp8q_version")
 
@@ -93,6 +97,20 @@ def load():
     lib.fp8q_gemm_workspace_size.restype = SZ
     lib.fp8q_gemm_noalloc.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, P]
     lib.fp8q_gemm_noalloc.restype = I
+    lib.fp8q_gemm_quant_a.argtypes = [P, P, P, P, P, P, I64, I64, I64, I, P, SZ, P]
+    lib.fp8q_gemm_quant_a.restype = I
+    lib.fp8q_ep_row_bytes.argtypes = [I64]
+    lib.fp8q_ep_row_bytes.restype = I64
+    lib.fp8q_ep_route.argtypes = [P, I64, I, I, P, P, P]
+    lib.fp8q_ep_route.restype = I
+    lib.fp8q_ep_pack.argtypes = [P, P, P, I64, I, I64, P, P]
+    lib.fp8q_ep_pack.restype = I
+    lib.fp8q_ep_unpack.argtypes = [P, I64, I64, P, P, I, P, P, I, P, P, I64, P]
+    lib.fp8q_ep_unpack.restype = I
+    lib.fp8q_ep_gather.argtypes = [P, I64, I64, I64, P, P, I, P, P]
+    lib.fp8q_ep_gather.restype = I
+    lib.fp8q_ep_combine.argtypes = [P, P, P, I64, I, I64, P, P]
+    lib.fp8q_ep_combine.restype = I
     lib.fp8q_selftest_wait.argtypes = [I64, P]
     lib.fp8q_selftest_wait.restype = I
     lib.fp8q_bench_mma_peak.argtypes = [I64, P]
@@ -346,6 +364,110 @@ def fp8q_gemm_noalloc(A8, sA, B8, sB, C, bscale=BSCALE_BLOCK128, stream=None):
         _stream(stream)))
 
 
+def fp8q_gemm_quant_a(A, B8, sB, C, A8_out=None, sA_out=None, ws=None, stream=None):
+    """GEMM on BF16 activations quantized 1x128 inside the kernel; optionally
+    also writes the quantized activations (A8_out [M][K] uint8, sA_out
+    [K/128][M] float32, both or neither)."""
+    if A.dim() != 2 or B8.dim() != 2:
+        raise ValueError("A must be [M][K] and B8 [N][K]")
+    M, K = A.shape
+    N, Kb_ = B8.shape
+    if Kb_ != K:
+        raise ValueError("A and B8 must have the same K (%d vs %d)" % (K, Kb_))
+    _shape(C, "C", (M, N))
+    _numel(sB, "sB", _scales(N) * _scales(K))
+    if (A8_out is None) != (sA_out is None):
+        raise ValueError("give both A8_out and sA_out, or neither")
+    if A8_out is not None:
+        _shape(A8_out, "A8_out", (M, K))
+        _numel(sA_out, "sA_out", _scales(K) * M)
+        pa, ps = _dev(A8_out, "A8_out", torch.uint8), _dev(sA_out, "sA_out", torch.float32)
+    else:
+        pa, ps = ctypes.c_void_p(None), ctypes.c_void_p(None)
+    wp, wn = _ws(ws)
+    _check("fp8q_gemm_quant_a", load().fp8q_gemm_quant_a(
+        _dev(A, "A", torch.bfloat16), _dev(B8, "B8", torch.uint8), _dev(sB, "sB", torch.float32),
+        _dev(C, "C"), pa, ps, M, N, K, _out_dtype(C.dtype), wp, wn, _stream(stream)))
+
+
+# ------------------------------------------- expert-parallel MoE data path
+def _opt(t, name, dtype=None):
+    """Device pointer of t, or NULL for an empty tensor (a rank may send or
+    receive no rows)."""
+    if t.numel() == 0:
+        return ctypes.c_void_p(None)
+    return _dev(t, name, dtype)
+
+
+def fp8q_ep_row_bytes(H: int) -> int:
+    n = int(load().fp8q_ep_row_bytes(int(H)))
+    if n < 0:
+        raise ValueError("H must be a positive multiple of 128")
+    return n
+
+
+def fp8q_ep_route(topk_ids, E, counts, pos, stream=None):
+    if topk_ids.dim() != 2:
+        raise ValueError("topk_ids must be [T][k]")
+    T, k = topk_ids.shape
+    _numel(counts, "counts", E)
+    _shape(pos, "pos", (T, k))
+    _check("fp8q_ep_route", load().fp8q_ep_route(
+        _dev(topk_ids, "topk_ids", torch.int32), T, k, int(E), _dev(counts, "counts", torch.int32),
+        _dev(pos, "pos", torch.int32), _stream(stream)))
+
+
+def fp8q_ep_pack(q, s, pos, send, stream=None):
+    T, H = q.shape
+    k = pos.shape[1] if pos.dim() == 2 else 1
+    _numel(s, "s", _scales(H) * T)
+    _shape(pos, "pos", (T, k))
+    _shape(send, "send", (T * k, fp8q_ep_row_bytes(H)))
+    _check("fp8q_ep_pack", load().fp8q_ep_pack(
+        _opt(q, "q", torch.uint8), _opt(s, "s", torch.float32), _opt(pos, "pos", torch.int32),
+        T, k, H, _opt(send, "send", torch.uint8), _stream(stream)))
+
+
+def fp8q_ep_unpack(recv, src_off, dest_base, m_offsets, rows_e, A8, sA, stream=None):
+    Mp, H = A8.shape
+    R = recv.shape[0]
+    nb = dest_base.numel()
+    El = rows_e.numel()
+    _shape(recv, "recv", (R, fp8q_ep_row_bytes(H)))
+    _numel(src_off, "src_off", nb + 1)
+    _numel(m_offsets, "m_offsets", El + 1)
+    _numel(sA, "sA", _scales(H) * Mp)
+    i64 = torch.int64
+    _check("fp8q_ep_unpack", load().fp8q_ep_unpack(
+        _opt(recv, "recv", torch.uint8), R, H, _dev(src_off, "src_off", i64),
+        _dev(dest_base, "dest_base", i64), nb, _dev(m_offsets, "m_offsets", i64),
+        _dev(rows_e, "rows_e", i64), El, _dev(A8, "A8", torch.uint8), _dev(sA, "sA", torch.float32),
+        Mp, _stream(stream)))
+
+
+def fp8q_ep_gather(Y, src_off, dest_base, out, stream=None):
+    Mp, N = Y.shape
+    R = out.shape[0]
+    nb = dest_base.numel()
+    _shape(out, "out", (R, N))
+    _numel(src_off, "src_off", nb + 1)
+    i64 = torch.int64
+    _check("fp8q_ep_gather", load().fp8q_ep_gather(
+        _dev(Y, "Y", torch.bfloat16), Mp, R, N, _dev(src_off, "src_off", i64),
+        _dev(dest_base, "dest_base", i64), nb, _opt(out, "out", torch.bfloat16), _stream(stream)))
+
+
+def fp8q_ep_combine(back, pos, w, out, stream=None):
+    T, k = pos.shape
+    N = out.shape[1]
+    _shape(back, "back", (T * k, N))
+    _shape(w, "w", (T, k))
+    _shape(out, "out", (T, N))
+    _check("fp8q_ep_combine", load().fp8q_ep_combine(
+        _opt(back, "back", torch.bfloat16), _opt(pos, "pos", torch.int32),
+        _opt(w, "w", torch.float32), T, k, N, _opt(out, "out", torch.bfloat16), _stream(stream)))
+
+
 def fp8q_gemm_workspace_size() -> int:
     return int(load().fp8q_gemm_workspace_size())
 
@@ -474,6 +596,20 @@ def gemm(A8, sA, B8, sB, out_dtype=torch.bfloat16, bscale=BSCALE_BLOCK128, strea
     ws = workspace(A8.device, stream) if stream_k else None
     fp8q_gemm_ws(A8, sA, B8, sB, C, bscale, ws, stream)
     return C
+
+
+def gemm_quant_a(A, B8, sB, out_dtype=torch.bfloat16, emit=True, stream=None, stream_k=True):
+    """C = quant_1x128(A) @ dequant(B8)^T with the quantization inside the GEMM.
+    Returns C, or (C, A8, sA) when emit is true."""
+    M, K = A.shape
+    C = torch.empty((M, B8.shape[0]), dtype=out_dtype, device=A.device)
+    A8 = sA = None
+    if emit:
+        A8 = torch.empty((M, K), dtype=torch.uint8, device=A.device)
+        sA = torch.empty((_scales(K), M), dtype=torch.float32, device=A.device)
+    ws = workspace(A.device, stream) if stream_k else None
+    fp8q_gemm_quant_a(A, B8, sB, C, A8, sA, ws, stream)
+    return (C, A8, sA) if emit else C
 
 
 def gemm_grouped(A8, sA, B8, sB, m_offsets, out_dtype=torch.bfloat16, stream=None,

@@ -14,6 +14,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "ep.cuh"
 #include "fp8q.h"
 #include "gemm.cuh"
 #include "quant.cuh"
@@ -113,6 +114,7 @@ struct DeviceState {
     int num_sms = 0;
     int* status = nullptr;            // device address of g_status on this device
     bool gemm_attr[2][2][2] = {};     // dynamic-smem attribute set, per kernel instance
+    bool gemm_qa_attr[2] = {};        // the same for the in-kernel-quantization GEMM
     bool quant_attr[2][2] = {};       // the same for the staged quantizers [kind][bf16 input]
     uint8_t* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch
     bool peak_attr = false;              // dynamic-smem attribute of k_mma_peak set
@@ -250,12 +252,12 @@ int quant_common(int kind, const void* x, int in_dtype, int64_t rows, int64_t co
 template <typename T> struct KQt { static constexpr auto fn = k_quant_128x1<T>; };
 template <typename T> struct KQw { static constexpr auto fn = k_quant_128x128<T>; };
 
-template <int BN, bool kRowB, bool kBf16>
+template <int BN, bool kRowB, bool kBf16, bool kQA = false>
 int launch_gemm_inst(DeviceState* d, const CUtensorMap& ta, const CUtensorMap& tb,
                      const CUtensorMap& tc, const GemmArgs& args, int tiles_upper, cudaStream_t st) {
-    using S = GemmShape<BN>;
-    auto kern = k_gemm<BN, kRowB, kBf16>;
-    bool& attr = d->gemm_attr[BN == 256][kRowB][kBf16];
+    using S = GemmShape<BN, kQA>;
+    auto kern = k_gemm<BN, kRowB, kBf16, kQA>;
+    bool& attr = kQA ? d->gemm_qa_attr[kBf16] : d->gemm_attr[BN == 256][kRowB][kBf16];
     if (!attr) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  S::kSmemBytes) != cudaSuccess)
@@ -298,6 +300,7 @@ struct GemmPlan {
     int BN = 256;
     int tiles_upper = 1;
     bool row_b = false, bf16 = false;
+    bool qa = false;                  // A quantized inside the GEMM (BF16 input)
 };
 
 // Checks that need neither a device nor the SM count.
@@ -358,10 +361,47 @@ int gemm_plan(const uint8_t* A8, const float* sA, const uint8_t* B8, const float
                     : tiles > (int64_t(1) << 30) ? (1 << 30) : static_cast<int>(tiles);
     p.row_b = bscale == FP8Q_BSCALE_ROW1x128;
     p.bf16 = out_dtype == FP8Q_BF16;
+    a.Abf = nullptr;
+    a.sA_out = nullptr;
+    return FP8Q_OK;
+}
+
+// Plan of the GEMM that quantizes its BF16 activations itself
+// (fp8q_gemm_quant_a): the same checks and schedule, 256-column tiles,
+// 128x128-block weight scales; tmA becomes the store map of the emitted A8
+// (boxes of 128 bytes x 32 rows, the quantizer warps' slices).
+int gemm_plan_qa(const void* Abf, const uint8_t* B8, const float* sB, void* C, uint8_t* A8_out,
+                 float* sA_out, int64_t M, int64_t N, int64_t K, int out_dtype, void* workspace,
+                 size_t ws_bytes, GemmPlan& p) {
+    if (!Abf) return FP8Q_ERR_INVALID_ARG;
+    if ((A8_out == nullptr) != (sA_out == nullptr)) return FP8Q_ERR_INVALID_ARG;
+    if (A8_out && !aligned(A8_out, 16)) return FP8Q_ERR_MISALIGNED;
+    if (sA_out && !aligned(sA_out, 4)) return FP8Q_ERR_MISALIGNED;
+    // the generic checks, with the BF16 input standing in for A8 and sA
+    // (both must be 16-byte aligned, which Abf has to be anyway)
+    const uint8_t* a8 = static_cast<const uint8_t*>(Abf);
+    const float* sa = static_cast<const float*>(Abf);
+    int rc = gemm_check_args(a8, sa, B8, sB, C, 1, M, N, K, out_dtype, FP8Q_BSCALE_BLOCK128);
+    if (rc != FP8Q_OK) return rc;
+    if (N % 256) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    rc = gemm_plan(a8, sa, B8, sB, C, nullptr, 1, M, N, K, out_dtype, FP8Q_BSCALE_BLOCK128,
+                   workspace, ws_bytes, p);
+    if (rc != FP8Q_OK) return rc;
+    std::memset(&p.ta, 0, sizeof(p.ta));
+    if (A8_out && (rc = encode_kmajor(&p.ta, A8_out, K, M, 32)) != FP8Q_OK) return rc;
+    p.args.sA = nullptr;
+    p.args.Abf = static_cast<const uint16_t*>(Abf);
+    p.args.sA_out = sA_out;
+    p.qa = true;
     return FP8Q_OK;
 }
 
 int gemm_launch(const GemmPlan& p, cudaStream_t st) {
+    if (p.qa)
+        return p.bf16 ? launch_gemm_inst<256, false, true, true>(p.d, p.ta, p.tb, p.tc, p.args,
+                                                                 p.tiles_upper, st)
+                      : launch_gemm_inst<256, false, false, true>(p.d, p.ta, p.tb, p.tc, p.args,
+                                                                  p.tiles_upper, st);
     return p.BN == 256 ? launch_gemm_bn<256>(p.d, p.ta, p.tb, p.tc, p.args, p.tiles_upper,
                                              p.row_b, p.bf16, st)
                        : launch_gemm_bn<128>(p.d, p.ta, p.tb, p.tc, p.args, p.tiles_upper,
@@ -551,6 +591,16 @@ int fp8q_gemm_grouped(const uint8_t* A8, const float* sA, const uint8_t* B8, con
                        FP8Q_BSCALE_BLOCK128, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int fp8q_gemm_quant_a(const void* A, const uint8_t* B8, const float* sB, void* C,
+                      uint8_t* A8_out, float* sA_out, int64_t M, int64_t N, int64_t K,
+                      int out_dtype, void* workspace, size_t workspace_bytes,
+                      fp8q_stream_t stream) {
+    GemmPlan p;
+    const int rc = gemm_plan_qa(A, B8, sB, C, A8_out, sA_out, M, N, K, out_dtype, workspace,
+                                workspace_bytes, p);
+    return rc != FP8Q_OK ? rc : gemm_launch(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int fp8q_gemm_noalloc(const uint8_t* A8, const float* sA, const uint8_t* B8, const float* sB,
                       void* C, int64_t M, int64_t N, int64_t K, int out_dtype, int bscale,
                       fp8q_stream_t stream) {
@@ -585,6 +635,97 @@ int fp8q_gemm_grouped_ws(const uint8_t* A8, const float* sA, const uint8_t* B8, 
     return gemm_common(A8, sA, B8, sB, C, m_offsets, G, M_total, N, K, out_dtype,
                        FP8Q_BSCALE_BLOCK128, workspace, workspace_bytes,
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+int64_t fp8q_ep_row_bytes(int64_t H) { return (H > 0 && H % 128 == 0) ? ep_row_bytes(H) : -1; }
+
+int fp8q_ep_route(const int32_t* topk_ids, int64_t T, int k, int E, int32_t* counts,
+                  int32_t* pos, fp8q_stream_t stream) {
+    if (!counts || (T > 0 && (!topk_ids || !pos))) return FP8Q_ERR_INVALID_ARG;
+    if (T < 0 || k < 1 || E < 1) return FP8Q_ERR_INVALID_ARG;
+    if (E > kEpMaxExperts || T * k > 0x7fffffff) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(topk_ids, 4) || !aligned(counts, 4) || !aligned(pos, 4)) return FP8Q_ERR_MISALIGNED;
+    // T == 0 still launches: the counts are written (all zero)
+    DeviceState* d = nullptr;
+    const int rc = device_state(&d);
+    if (rc != FP8Q_OK) return rc;
+    k_ep_route<<<1, kEpRouteThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        topk_ids, T * k, E, counts, pos, d->status);
+    return launched();
+}
+
+int fp8q_ep_pack(const uint8_t* q, const float* s, const int32_t* pos, int64_t T, int k,
+                 int64_t H, uint8_t* send, fp8q_stream_t stream) {
+    if (T < 0 || k < 1 || H <= 0) return FP8Q_ERR_INVALID_ARG;
+    if (T == 0) return FP8Q_OK;
+    if (!q || !s || !pos || !send) return FP8Q_ERR_INVALID_ARG;
+    if (H % 128 || T * k > 0x7fffffff) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(q, 16) || !aligned(send, 16) || !aligned(s, 4) || !aligned(pos, 4))
+        return FP8Q_ERR_MISALIGNED;
+    k_ep_pack<<<static_cast<unsigned>((T * k + 7) / 8), 256, 0,
+                reinterpret_cast<cudaStream_t>(stream)>>>(q, s, pos, T, k, H, send);
+    return launched();
+}
+
+int fp8q_ep_unpack(const uint8_t* recv, int64_t R, int64_t H, const int64_t* src_off,
+                   const int64_t* dest_base, int nb, const int64_t* m_offsets,
+                   const int64_t* rows_e, int El, uint8_t* A8, float* sA, int64_t Mp,
+                   fp8q_stream_t stream) {
+    if (!src_off || !dest_base || !m_offsets || !rows_e || !A8 || !sA) return FP8Q_ERR_INVALID_ARG;
+    if (R < 0 || H <= 0 || nb < 1 || El < 1 || Mp <= 0 || (R > 0 && !recv))
+        return FP8Q_ERR_INVALID_ARG;
+    if (H % 128 || Mp % 128 || R > 0x7fffffffLL * 8 || El > 65535) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if ((recv && !aligned(recv, 16)) || !aligned(A8, 16) || !aligned(sA, 4) ||
+        !aligned(src_off, 8) || !aligned(dest_base, 8) || !aligned(m_offsets, 8) ||
+        !aligned(rows_e, 8))
+        return FP8Q_ERR_MISALIGNED;
+    DeviceState* d = nullptr;
+    const int rc = device_state(&d);
+    if (rc != FP8Q_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (R > 0)
+        k_ep_unpack<<<static_cast<unsigned>((R + 7) / 8), 256, 0, st>>>(
+            recv, R, H, src_off, dest_base, nb, A8, sA, Mp, d->status);
+    if (cudaGetLastError() != cudaSuccess) return cuda_fail();
+    k_ep_zero_pad<<<dim3(static_cast<unsigned>(El), 16), 256, 0, st>>>(m_offsets, rows_e, H, A8,
+                                                                        sA, Mp, d->status);
+    return launched();
+}
+
+int fp8q_ep_gather(const void* Y, int64_t Mp, int64_t R, int64_t N, const int64_t* src_off,
+                   const int64_t* dest_base, int nb, void* out, fp8q_stream_t stream) {
+    if (R < 0 || N <= 0 || nb < 1 || Mp < 0) return FP8Q_ERR_INVALID_ARG;
+    if (R == 0) return FP8Q_OK;
+    if (!Y || !src_off || !dest_base || !out) return FP8Q_ERR_INVALID_ARG;
+    if (N % 8 || R > 0x7fffffffLL * 8) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(Y, 16) || !aligned(out, 16) || !aligned(src_off, 8) || !aligned(dest_base, 8))
+        return FP8Q_ERR_MISALIGNED;
+    DeviceState* d = nullptr;
+    const int rc = device_state(&d);
+    if (rc != FP8Q_OK) return rc;
+    k_ep_gather<<<static_cast<unsigned>((R + 7) / 8), 256, 0,
+                  reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __nv_bfloat16*>(Y), R, N, src_off, dest_base, nb, Mp,
+        static_cast<__nv_bfloat16*>(out), d->status);
+    return launched();
+}
+
+int fp8q_ep_combine(const void* back, const int32_t* pos, const float* w, int64_t T, int k,
+                    int64_t N, void* out, fp8q_stream_t stream) {
+    if (T < 0 || k < 1 || N <= 0) return FP8Q_ERR_INVALID_ARG;
+    if (T == 0) return FP8Q_OK;
+    if (!pos || !w || !out || !back) return FP8Q_ERR_INVALID_ARG;
+    if (N % 8 || T > 0x7fffffff || (N + 2047) / 2048 > 65535) return FP8Q_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(back, 16) || !aligned(out, 16) || !aligned(pos, 4) || !aligned(w, 4))
+        return FP8Q_ERR_MISALIGNED;
+    DeviceState* d = nullptr;
+    const int rc = device_state(&d);
+    if (rc != FP8Q_OK) return rc;
+    const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((N + 2047) / 2048));
+    k_ep_combine<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __nv_bfloat16*>(back), pos, w, T, k, N, static_cast<__nv_bfloat16*>(out),
+        d->status);
+    return launched();
 }
 
 int fp8q_get_device_status(fp8q_stream_t stream) {
@@ -644,6 +785,7 @@ const char* fp8q_status_string(int status) {
         case FP8Q_ERR_CUDA: return "CUDA error";
         case FP8Q_ERR_TIMEOUT: return "device pipeline wait timed out";
         case FP8Q_ERR_BAD_GROUPS: return "invalid group offsets";
+        case FP8Q_ERR_BAD_ROUTING: return "expert id out of range";
         default: return "unknown status";
     }
 }

@@ -31,6 +31,7 @@
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
+#include "quant.cuh"   // group_scale: the scale rule of the in-kernel quantizer
 
 namespace fp8q {
 
@@ -50,19 +51,33 @@ constexpr int kMaxGroups = 512;
 #ifndef FP8Q_MMA_WARP
 #define FP8Q_MMA_WARP 1
 #endif
-template <int BN>
+//
+// With kQA (activations quantized inside the GEMM), warpgroup 1 is the
+// quantizer: thread q converts row q of the A tile of each K block from BF16
+// to E4M3 (1x128 scale rule) straight into the operand stage, and the
+// promotion warpgroups move up by one.  Registers per lane then split
+// 32 (control) + 96 (quantizer) + 2 * 192 (promotion) = 512.
+template <int BN, bool kQA = false>
 struct GemmShape {
     static constexpr int kHalves = BN / 128;             // 128-column halves of the tile
     static constexpr int kPromoWarps = 4 * kHalves;
     static constexpr int kProducerWarp = 0;
     static constexpr int kMmaWarp = FP8Q_MMA_WARP;
-    static constexpr int kFirstPromoWarp = 4;
-    static constexpr int kThreads = 128 * (1 + kHalves);
+    static constexpr int kFirstQuantWarp = 4;
+    static constexpr int kFirstPromoWarp = kQA ? 8 : 4;
+    static constexpr int kThreads = 128 * (1 + kHalves + (kQA ? 1 : 0));
     static constexpr bool kRealloc = kHalves > 1;
-    static constexpr int kCtrlRegs = 56;
-    static constexpr int kPromoRegs = 224;
-    static_assert(!kRealloc || 128 * kCtrlRegs + 128 * kHalves * kPromoRegs <= kThreads * 168,
+    static constexpr int kCtrlRegs = kQA ? 32 : 56;
+    static constexpr int kQuantRegs = 96;
+    static constexpr int kPromoRegs = kQA ? 192 : 224;
+    static constexpr int kLaunchRegs = (65536 / kThreads) & ~7;
+    static_assert(!kRealloc || 128 * kCtrlRegs + (kQA ? 128 * kQuantRegs : 0) +
+                                       128 * kHalves * kPromoRegs <= kThreads * kLaunchRegs,
                   "register split exceeds the launch allocation");
+    static_assert(!kQA || kRealloc, "in-kernel quantization needs the 256-column tile");
+    // arrivals completing a stage: the producer's (with the TMA byte count),
+    // plus one per quantizer warp
+    static constexpr int kFullArrivals = 1 + (kQA ? 4 : 0);
     static_assert(kMmaWarp > 0 && kMmaWarp < 4, "MMA warp must be a control warp");
     static constexpr int kStages = BN == 256 ? 3 : 5;
     static constexpr int kABytes = kBM * kBK;
@@ -98,6 +113,9 @@ struct GemmArgs {
     int* status;
     float* ws;              // stream-K partial tiles, or nullptr (whole tiles only)
     int* counters;          // stream-K arrival counters, zero between calls
+    const uint16_t* Abf;    // in-kernel quantization: BF16 activations [M_total][K]
+    float* sA_out;          // in-kernel quantization: emitted 1x128 scales [K/128][M_total]
+                            // (nullptr: none; A8 goes out through the tmA store map)
 };
 
 // ------------------------------------------------------------ work schedule
@@ -218,6 +236,60 @@ __device__ __forceinline__ void promote_chunk(float2* acc, const uint32_t (&r)[W
     }
 }
 
+// Columns of the partial per tcgen05.ld in the promotion loop (block-scaled
+// and row-scaled B).  tcgen05.wait::ld waits for every load the thread has
+// in flight, so each wait costs one load latency: wider loads mean fewer
+// waits before the TMEM buffer can go back to the MMA warp.
+#ifndef FP8Q_PROMO_W
+#define FP8Q_PROMO_W 16
+#endif
+#ifndef FP8Q_PROMO_W_ROW
+#define FP8Q_PROMO_W_ROW 8
+#endif
+
+// One promotion warp's share of a 128-K block: the thread's 128 columns of
+// the TMEM partial, scaled and added into acc.  W < 64: chunks of W columns
+// with the next chunk's load in flight while the current one is scaled.
+// W = 64: two loads of 64 columns into one register buffer.  The TMEM buffer
+// goes back to the MMA warp (one arrive per warp on free_bar) as soon as the
+// last load has landed, before that chunk is accumulated.
+template <bool kRowB, int W>
+__device__ __forceinline__ void promote_block(float2* acc, uint32_t taddr, float f, float fa,
+                                              const float* sbc, uint64_t* free_bar, int lane) {
+    if constexpr (W == 64) {
+        uint32_t r[64];
+        tmem_ld_chunk(taddr, r);
+        tmem_ld_wait(r);
+        promote_chunk<kRowB>(acc, r, f, fa, sbc);
+        tmem_ld_chunk(taddr + 64, r);
+        tmem_ld_wait(r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(free_bar);
+        promote_chunk<kRowB>(acc + 32, r, f, fa, sbc + 64);
+    } else {
+        constexpr int kC = 128 / W;
+        uint32_t r0[W], r1[W];
+        tmem_ld_chunk(taddr, r0);
+        tmem_ld_wait(r0);
+#pragma unroll
+        for (int c = 0; c < kC; c += 2) {
+            tmem_ld_chunk(taddr + (c + 1) * W, r1);
+            promote_chunk<kRowB>(acc + c * (W / 2), r0, f, fa, sbc + c * W);
+            tmem_ld_wait(r1);
+            if (c + 2 < kC) {
+                tmem_ld_chunk(taddr + (c + 2) * W, r0);
+            } else {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(free_bar);
+            }
+            promote_chunk<kRowB>(acc + (c + 1) * (W / 2), r1, f, fa, sbc + (c + 1) * W);
+            if (c + 2 < kC) tmem_ld_wait(r0);
+        }
+    }
+}
+
 // Tile t -> A row of the tile, B row (in the [G*N] view), first column, group.
 struct TileCoord {
     int arow, brow, n0, e;
@@ -296,11 +368,84 @@ __device__ __forceinline__ void store_tile_tma(const float2* acc, uint8_t* stg,
     }
 }
 
-template <int BN, bool kRowB, bool kBf16Out>
-__global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
+// In-kernel 1x128 quantization of the A tile (128 rows x 128 K) of one K
+// block, by the quantizer warpgroup.  Warp qw owns rows 32 qw .. 32 qw + 31
+// of the tile; it handles them in two halves of 16 rows, in 8 passes of two
+// rows each: in pass p of half hf, half-warp h (lanes 16h .. 16h + 15) holds
+// row 32 qw + 16 hf + 2p + h, lane l of it the 16-byte chunk of 8 BF16
+// values at columns 8 (l % 16) .. +7 -- so each load instruction reads two
+// whole 256-byte rows.  A half is loaded (qa_load_half) one half ahead of
+// its conversion (qa_convert_half), so the global loads overlap the
+// conversion of the previous half.
+__device__ __forceinline__ void qa_load_half(uint4 (&v)[8], const uint16_t* rows, int64_t K,
+                                             int kb, int hf, int lane) {
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const int r = hf * 16 + 2 * p + (lane >> 4);           // row within the warp's 32
+        v[p] = __ldg(reinterpret_cast<const uint4*>(rows + r * K + kb * kBK + (lane & 15) * 8));
+    }
+}
+
+// Converts one half (16 rows) into the stage's A tile, with the 128-byte
+// swizzle a TMA load of the A8 tile would have produced (16-byte chunk j of
+// row r at j ^ (r % 8)), and stores the 16 rows' scales to slot[] (and
+// sa_out[], if given), both indexed by the row within the tile.  The scale
+// rule is the quantizers': amax is exact (the largest BF16 magnitude, found
+// as the largest 15-bit magnitude field, whose order equals that of the
+// finite values), s = amax / 448 and inv = 448 / amax are correctly rounded,
+// the cast rounds to nearest even and saturates.  Each row's maximum is
+// reduced over its half-warp; the 16 maxima are then gathered onto lanes
+// 0..15, which compute one row's scale each, and the inverses are
+// broadcast back.
+__device__ __forceinline__ void qa_convert_half(const uint4 (&v)[8], uint8_t* tile, float* slot,
+                                                float* sa_out, int qw, int hf, int lane) {
+    float mine = 0.0f;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        uint32_t m = __vmaxu2(__vmaxu2(v[p].x & 0x7FFF7FFFu, v[p].y & 0x7FFF7FFFu),
+                              __vmaxu2(v[p].z & 0x7FFF7FFFu, v[p].w & 0x7FFF7FFFu));
+        m = (m & 0xFFFFu) > (m >> 16) ? (m & 0xFFFFu) : (m >> 16);
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        const uint32_t t = __shfl_sync(0xffffffffu, m, (lane & 1) << 4);
+        if ((lane >> 1) == p) mine = __uint_as_float(t << 16);
+    }
+    float sc, inv_l;
+    group_scale(mine, sc, inv_l);                  // lane j < 16: row 16 hf + j of the warp
+    if (lane < 16) {
+        const int r = qw * 32 + hf * 16 + lane;
+        slot[r] = sc;
+        if (sa_out) sa_out[r] = sc;
+    }
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const float inv = __shfl_sync(0xffffffffu, inv_l, 2 * p + (lane >> 4));
+        const int r = qw * 32 + hf * 16 + 2 * p + (lane >> 4);
+        const uint32_t w[4] = {v[p].x, v[p].y, v[p].z, v[p].w};
+        uint32_t o[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t lo = cvt_e4m3x2(__fmul_rn(__uint_as_float(w[2 * h] << 16), inv),
+                                           __fmul_rn(__uint_as_float(w[2 * h] & 0xFFFF0000u), inv));
+            const uint32_t hi = cvt_e4m3x2(__fmul_rn(__uint_as_float(w[2 * h + 1] << 16), inv),
+                                           __fmul_rn(__uint_as_float(w[2 * h + 1] & 0xFFFF0000u), inv));
+            o[h] = lo | (hi << 16);
+        }
+        const int li = lane & 15;
+        *reinterpret_cast<uint2*>(tile + r * 128 + ((((li >> 1) ^ (r & 7))) << 4) + (li & 1) * 8) =
+            make_uint2(o[0], o[1]);
+    }
+}
+
+template <int BN, bool kRowB, bool kBf16Out, bool kQA = false>
+__global__ void __launch_bounds__(GemmShape<BN, kQA>::kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
-    using S = GemmShape<BN>;
+    using S = GemmShape<BN, kQA>;
+    static_assert(!(kQA && kRowB), "in-kernel quantization is for 128x128-block weights");
+    constexpr bool kSlots = kRowB || kQA;     // per-block scales go through the slot ring
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -324,12 +469,12 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
     if (threadIdx.x == 0) {
 #pragma unroll 1
         for (int i = 0; i < S::kStages; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], S::kFullArrivals);
             mbar_init(&empty[i], 1);
         }
 #pragma unroll 1
         for (int i = 0; i < kScaleSlots; ++i) {
-            mbar_init(&sfull[i], 1);
+            mbar_init(&sfull[i], kQA ? 4 : 1);
             mbar_init(&sempty[i], S::kPromoWarps);
         }
 #pragma unroll 1
@@ -377,7 +522,8 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
     const uint32_t tmem_base = misc[0];
     const Sched& sched = *sched_smem;        // read from shared memory where used
 
-    if (warp < S::kFirstPromoWarp) {
+    if (warp < 4) {
+        // ----------------------------------------------------- control
         if (S::kRealloc) setmaxnreg_dec<S::kCtrlRegs>();
         if (warp == S::kProducerWarp && lane == 0) {
             // -------------------------------------------------- producer
@@ -393,8 +539,13 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, args.status)) { ok = false; break; }
                     uint8_t* sa = smem + stage * S::kStageBytes;
-                    mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
-                    tma_load_2d(sa, &tmA, &full[stage], kb * kBK, tc.arow);
+                    if (kQA) {
+                        // the quantizer warps write the A tile; TMA brings B
+                        mbar_arrive_expect_tx(&full[stage], S::kBBytes);
+                    } else {
+                        mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
+                        tma_load_2d(sa, &tmA, &full[stage], kb * kBK, tc.arow);
+                    }
                     tma_load_2d(sa + S::kABytes, &tmB, &full[stage], kb * kBK, tc.brow);
                     if (++stage == S::kStages) { stage = 0; phase ^= 1; }
 
@@ -459,6 +610,67 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
             tc_fence_after();
             tmem_dealloc(tmem_base, S::kTmemCols);
         }
+    } else if (kQA && warp < S::kFirstPromoWarp) {
+        // ----------------------------------------------------- quantizer
+        // Warp qw converts rows 32 qw .. 32 qw + 31 of every A tile into the
+        // operand stage (qa_convert_half), puts their scales in the slot ring
+        // for the promotion warps and, when the call emits the stored
+        // activations and this is the tile of column 0 (so that every block
+        // is emitted once), also into sA_out; lane 0 then copies the warp's
+        // 32 rows of E4M3 bytes out with a TMA store from the stage, whose
+        // layout is that of the A8 tensor map.  The next block's rows are
+        // loaded while the current one is converted.
+        setmaxnreg_dec<S::kQuantRegs>();
+        const int qw = warp - S::kFirstQuantWarp;
+        uint32_t stage = 0, phase = 0, slot = 0, sphase = 0;
+        bool ok = true;
+        SegIter si;
+        si.start(sched_smem, blockIdx.x);
+        Seg sg;
+#pragma unroll 1
+        while (ok && si.next(sg)) {
+            const TileCoord tc = decode_tile<BN>(sg.t, grouped, N, args.G, gtile, grow);
+            const bool emit = args.sA_out != nullptr && tc.n0 == 0;
+            const uint16_t* rows = args.Abf + static_cast<size_t>(tc.arow + qw * 32) * args.K;
+            uint4 va[8], vb[8];
+            qa_load_half(va, rows, args.K, sg.kb0, 0, lane);
+            qa_load_half(vb, rows, args.K, sg.kb0, 1, lane);
+#pragma unroll 1
+            for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1, args.status)) ||
+                    !__all_sync(0xffffffffu, mbar_wait(&sempty[slot], sphase ^ 1, args.status))) {
+                    ok = false;
+                    break;
+                }
+                // Every block commits one bulk group (empty unless it emits),
+                // so waiting until kStages - 1 groups are pending means the
+                // store of the block that last used this stage has read it.
+                if (lane == 0) bulk_wait_read_pending<S::kStages - 1>();
+                __syncwarp();
+                uint8_t* tile = smem + stage * S::kStageBytes;
+                float* sl = reinterpret_cast<float*>(smem + S::kOffScale + slot * S::kSlotBytes);
+                float* so = emit ? args.sA_out + static_cast<size_t>(kb) * args.M_total + tc.arow
+                                 : nullptr;
+                qa_convert_half(va, tile, sl, so, qw, 0, lane);
+                if (kb + 1 < sg.kb1) qa_load_half(va, rows, args.K, kb + 1, 0, lane);
+                qa_convert_half(vb, tile, sl, so, qw, 1, lane);
+                if (kb + 1 < sg.kb1) qa_load_half(vb, rows, args.K, kb + 1, 1, lane);
+                fence_proxy_async_smem();          // the MMA reads the tile through the async proxy
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&full[stage]);
+                    mbar_arrive(&sfull[slot]);
+                    if (emit) tma_store_2d(&tmA, tile + qw * 4096, kb * kBK, tc.arow + qw * 32);
+                    bulk_commit_group();
+                }
+                if (++stage == S::kStages) { stage = 0; phase ^= 1; }
+                if (++slot == kScaleSlots) { slot = 0; sphase ^= 1; }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+        tc_fence_before();
+        cta_barrier(S::kThreads);
     } else {
         // ----------------------------------------------------- promotion
         if (S::kRealloc) setmaxnreg_inc<S::kPromoRegs>();
@@ -481,7 +693,7 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
                 args.sB + (static_cast<size_t>(tc.e) * (N / 128) + (tc.n0 / 128 + half)) * Kb;
             float fa_next = 0.0f, fb_next = 0.0f;
             if (!kRowB) {
-                fa_next = __ldg(sa_row + static_cast<size_t>(sg.kb0) * args.M_total);
+                if (!kQA) fa_next = __ldg(sa_row + static_cast<size_t>(sg.kb0) * args.M_total);
                 fb_next = __ldg(sb_blk + sg.kb0);
             }
 #pragma unroll
@@ -490,8 +702,17 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
             for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
                 const uint32_t b = it % S::kTbufs, tph = (it / S::kTbufs) & 1;
                 float fa, f;
-                const float* sbc = nullptr;
-                if (!kRowB) {
+                const float* sbc = reinterpret_cast<const float*>(smem);   // read only if kRowB
+                if (kQA) {
+                    // the row scale comes from the quantizer warps' slot ring
+                    if (!__all_sync(0xffffffffu, mbar_wait(&sfull[slot], sphase, args.status))) {
+                        ok = false;
+                        break;
+                    }
+                    fa = reinterpret_cast<const float*>(smem + S::kOffScale + slot * S::kSlotBytes)[row];
+                    f = fa * fb_next;
+                    if (kb + 1 < sg.kb1) fb_next = __ldg(sb_blk + kb + 1);
+                } else if (!kRowB) {
                     fa = fa_next;
                     f = fa_next * fb_next;
                     if (kb + 1 < sg.kb1) {
@@ -516,51 +737,9 @@ __global__ void __launch_bounds__(GemmShape<BN>::kThreads, 1)
                 tc_fence_after();
                 const uint32_t taddr =
                     tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * BN + half * 128;
-                if (!kRowB) {
-                    // Sixteen-column chunks, the next chunk's load in flight while
-                    // the current one is scaled; the TMEM buffer goes back to the
-                    // MMA warp as soon as the last chunk has arrived.
-                    uint32_t r0[16], r1[16];
-                    tmem_ld_chunk(taddr, r0);
-                    tmem_ld_wait(r0);
-#pragma unroll
-                    for (int c = 0; c < 8; c += 2) {
-                        tmem_ld_chunk(taddr + (c + 1) * 16, r1);
-                        promote_chunk<false>(acc + c * 8, r0, f, fa, nullptr);
-                        tmem_ld_wait(r1);
-                        if (c + 2 < 8) {
-                            tmem_ld_chunk(taddr + (c + 2) * 16, r0);
-                        } else {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&tempty[b]);
-                        }
-                        promote_chunk<false>(acc + (c + 1) * 8, r1, f, fa, nullptr);
-                        if (c + 2 < 8) tmem_ld_wait(r0);
-                    }
-                } else {
-                    // Eight-column chunks, the next chunk's load in flight while
-                    // the current one is scaled.
-                    uint32_t r0[8], r1[8];
-                    tmem_ld_chunk(taddr, r0);
-                    tmem_ld_wait(r0);
-#pragma unroll
-                    for (int c = 0; c < 16; c += 2) {
-                        tmem_ld_chunk(taddr + (c + 1) * 8, r1);
-                        promote_chunk<true>(acc + c * 4, r0, f, fa, sbc + c * 8);
-                        tmem_ld_wait(r1);
-                        if (c + 2 < 16) {
-                            tmem_ld_chunk(taddr + (c + 2) * 8, r0);
-                        } else {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&tempty[b]);
-                        }
-                        promote_chunk<true>(acc + (c + 1) * 4, r1, f, fa, sbc + (c + 1) * 8);
-                        if (c + 2 < 16) tmem_ld_wait(r0);
-                    }
-                }
-                if (kRowB) {
+                promote_block<kRowB, (kRowB ? FP8Q_PROMO_W_ROW : FP8Q_PROMO_W)>(
+                    acc, taddr, f, fa, sbc, &tempty[b], lane);
+                if (kSlots) {
                     // the slot was read with generic loads and is refilled by the
                     // async proxy (a bulk copy): order the reads before that write
                     fence_proxy_async_smem();

@@ -144,6 +144,13 @@ __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Waits until at most N of the bulk-store groups this thread committed are
+// still reading their shared-memory sources (groups complete in order).
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_pending() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
 // Waits until every bulk store this thread committed has completed.
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");

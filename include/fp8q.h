@@ -62,8 +62,9 @@ typedef enum {
     FP8Q_ERR_MISALIGNED = 3,       /* a pointer is not 16-byte aligned */
     FP8Q_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed */
     FP8Q_ERR_TIMEOUT = 5,          /* device: a pipeline wait exceeded its limit */
-    FP8Q_ERR_BAD_GROUPS = 6        /* device: m_offsets not monotone / not multiples of 128 /
+    FP8Q_ERR_BAD_GROUPS = 6,       /* device: m_offsets not monotone / not multiples of 128 /
                                       beyond M_total */
+    FP8Q_ERR_BAD_ROUTING = 7       /* device: an expert id outside [0, E) */
 } fp8q_status;
 
 typedef enum { FP8Q_F32 = 0, FP8Q_BF16 = 1 } fp8q_dtype;
@@ -229,6 +230,31 @@ FP8Q_API int fp8q_gemm_ws(const uint8_t* A8, const float* sA, const uint8_t* B8,
                  void* C, int64_t M, int64_t N, int64_t K, int out_dtype, int bscale,
                  void* workspace, size_t workspace_bytes, fp8q_stream_t stream);
 
+/* GEMM that quantizes its activations itself: the 1x128 quantization of the
+ * BF16 activations happens in the GEMM's producer stage, on the way from
+ * global to shared memory, instead of in a separate pass that writes A8 to
+ * HBM and reads it back -- woojincopolymer post, para. 4 (the FP8 cast fused
+ * with the global-to-shared transfer; the forward activations kept as 1x128
+ * FP8 tiles).  The result is that of fp8q_gemm_ws(A8, sA, B8, sB, C, ...)
+ * with (A8, sA) = fp8q_quant_act_1x128(A): the quantization follows the same
+ * rule bit for bit, and C the same tolerance.
+ *   A       [M][K] BF16 activations, 16-byte aligned
+ *   B8, sB  [N][K] E4M3 weights with 128x128 block scales [N/128][K/128]
+ *   C       [M][N] out_dtype (FP8Q_F32 or FP8Q_BF16), 16-byte aligned
+ *   A8_out  [M][K] uint8 (16-byte aligned) and sA_out [K/128][M] float32
+ *           (4-byte aligned), or both NULL: when given, the quantized
+ *           activations are also written there (the stored forward tiles),
+ *           identical to fp8q_quant_act_1x128's output.
+ *   workspace, workspace_bytes: the stream-K workspace, as for fp8q_gemm_ws
+ *           (NULL: whole tiles only).
+ * Requires N a multiple of 256, M and K multiples of 128, and the size
+ * limits of fp8q_gemm (FP8Q_ERR_UNSUPPORTED_SHAPE otherwise);
+ * FP8Q_ERR_INVALID_ARG if only one of A8_out, sA_out is given. */
+FP8Q_API int fp8q_gemm_quant_a(const void* A, const uint8_t* B8, const float* sB, void* C,
+                      uint8_t* A8_out, float* sA_out, int64_t M, int64_t N, int64_t K,
+                      int out_dtype, void* workspace, size_t workspace_bytes,
+                      fp8q_stream_t stream);
+
 /* fp8q_gemm_grouped with a stream-K workspace (same rules as fp8q_gemm_ws). */
 FP8Q_API int fp8q_gemm_grouped_ws(const uint8_t* A8, const float* sA, const uint8_t* B8,
                          const float* sB, void* C, const int* m_offsets, int G,
@@ -259,6 +285,77 @@ FP8Q_API int fp8q_gemm_grouped_ws(const uint8_t* A8, const float* sA, const uint
 FP8Q_API int fp8q_gemm_noalloc(const uint8_t* A8, const float* sA, const uint8_t* B8,
                       const float* sB, void* C, int64_t M, int64_t N, int64_t K, int out_dtype,
                       int bscale, fp8q_stream_t stream);
+
+/* ------------------------------------------ expert-parallel MoE data path */
+
+/* FP8 dispatch and BF16 combine around the grouped GEMM for experts spread
+ * over ranks: "Six Reasons...", para. 4 (the activations are quantized to
+ * FP8 before they are dispatched to the experts' up projection; the combine
+ * stays in BF16).  Experts are numbered rank-major: rank d owns experts
+ * d*E_local .. (d+1)*E_local - 1 of E = ranks * E_local.  A rank
+ *   1. quantizes its tokens x[T][H] per 1x128 tile (fp8q_quant_act_1x128);
+ *   2. fp8q_ep_route: counts per expert and, for every (token, slot), the
+ *      row it takes in the send order (expert-major, then token, then slot);
+ *   3. fp8q_ep_pack: one packed row per (token, slot) -- the token's H E4M3
+ *      bytes, then its H/128 FP32 scales, padded to fp8q_ep_row_bytes(H);
+ *   4. sends the rows of each destination's experts to it and receives, from
+ *      every source rank in turn, that rank's rows for each local expert
+ *      (an all-to-all of packed rows: the caller's collective);
+ *   5. fp8q_ep_unpack: received rows -> the grouped GEMM's A8 [Mp][H] and
+ *      sA [H/128][Mp], each local expert's rows contiguous and padded with
+ *      zero rows to a multiple of 128;
+ *   6. fp8q_gemm_grouped_ws with the local experts' weights -> Y [Mp][N] BF16;
+ *   7. fp8q_ep_gather: Y's rows back in the order they arrived, and the
+ *      reverse all-to-all returns them to their source ranks;
+ *   8. fp8q_ep_combine: out[t] = bf16(sum_j w[t][j] * y_tj), FP32 sum.
+ * The receive layout tables (per source and local expert: start of its rows
+ * in the receive order, src_off[b], and in A8, dest_base[b], b = w*E_local +
+ * e; per local expert: m_offsets and rows_e, the real row count) are small
+ * and made by the caller from the exchanged counts. */
+
+/* Bytes of one packed dispatch row for hidden size H (a multiple of 128):
+ * H + 4*H/128 rounded up to a multiple of 16.  -1 for an invalid H. */
+FP8Q_API int64_t fp8q_ep_row_bytes(int64_t H);
+
+/* topk_ids [T][k] int32 (device) -> counts [E] int32 and pos [T][k] int32:
+ * pos[t][j] = (rows of experts below e) + (entries of expert e before (t, j)
+ * in row-major order), e = topk_ids[t][j]; deterministic.  One CTA.
+ * Requires 1 <= E <= 256 and T*k < 2^31; an id outside [0, E) records
+ * FP8Q_ERR_BAD_ROUTING in the device status and nothing is written. */
+FP8Q_API int fp8q_ep_route(const int32_t* topk_ids, int64_t T, int k, int E, int32_t* counts,
+                  int32_t* pos, fp8q_stream_t stream);
+
+/* q [T][H] uint8, s [H/128][T] float32 (fp8q_quant_act_1x128's output),
+ * pos [T][k] -> send [T*k][fp8q_ep_row_bytes(H)]: row pos[t][j] gets token
+ * t's bytes and scales.  q and send 16-byte aligned; H a multiple of 128. */
+FP8Q_API int fp8q_ep_pack(const uint8_t* q, const float* s, const int32_t* pos, int64_t T, int k,
+                 int64_t H, uint8_t* send, fp8q_stream_t stream);
+
+/* recv [R][fp8q_ep_row_bytes(H)] -> A8 [Mp][H] uint8 and sA [H/128][Mp]
+ * float32: received row i of block b (src_off[b] <= i < src_off[b+1], nb
+ * blocks) goes to row dest_base[b] + i - src_off[b]; then the padding rows
+ * of each local expert e (m_offsets[e] + rows_e[e] .. m_offsets[e+1] - 1,
+ * fewer than 128) are zeroed.  Tables are DEVICE int64 arrays (src_off has
+ * nb + 1 entries, m_offsets El + 1).  Mp = m_offsets[El], a multiple of 128. */
+FP8Q_API int fp8q_ep_unpack(const uint8_t* recv, int64_t R, int64_t H, const int64_t* src_off,
+                   const int64_t* dest_base, int nb, const int64_t* m_offsets,
+                   const int64_t* rows_e, int El, uint8_t* A8, float* sA, int64_t Mp,
+                   fp8q_stream_t stream);
+
+/* Y [Mp][N] BF16 -> out [R][N] BF16 in the receive order: out[i] =
+ * Y[dest_base[b] + i - src_off[b]].  N a multiple of 8, 16-byte aligned.
+ * A table entry pointing outside Y's Mp rows records FP8Q_ERR_BAD_ROUTING
+ * and that row is skipped (the same holds for fp8q_ep_unpack's rows and
+ * fp8q_ep_combine's positions). */
+FP8Q_API int fp8q_ep_gather(const void* Y, int64_t Mp, int64_t R, int64_t N, const int64_t* src_off,
+                   const int64_t* dest_base, int nb, void* out, fp8q_stream_t stream);
+
+/* back [T*k][N] BF16 (the returned expert results, in the send order), pos
+ * [T][k], w [T][k] float32 gate weights -> out [T][N] BF16:
+ * out[t][n] = bf16(sum_{j=0..k-1} w[t][j] * back[pos[t][j]][n]), summed in
+ * FP32 in slot order, rounded to nearest even.  N a multiple of 8. */
+FP8Q_API int fp8q_ep_combine(const void* back, const int32_t* pos, const float* w, int64_t T,
+                    int k, int64_t N, void* out, fp8q_stream_t stream);
 
 /* ------------------------------------------------------------------ status */
 

@@ -209,3 +209,43 @@ def test_python_binding_checks_buffer_sizes(lib):
     with pytest.raises(ValueError, match="q must have shape"):
         fq.fp8q_rmsnorm_quant_1x128(x, torch.zeros(K, dtype=torch.bfloat16),
                                     torch.zeros(M + 128, K, dtype=u8), sA)
+
+
+def test_fused_quant_gemm_argument_checks(lib):
+    f = lib.fp8q_gemm_quant_a
+    f.argtypes = [P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                  P, ctypes.c_size_t, P]
+    bufs = (A16, A16b, A16c, P(0x40000))
+    assert f(None, *bufs[1:], None, None, 256, 256, 256, 0, None, 0, None) == 1      # no A
+    assert f(*bufs, A16, None, 256, 256, 256, 0, None, 0, None) == 1               # A8 without sA
+    assert f(*bufs, None, None, 256, 384, 256, 0, None, 0, None) == 2              # N % 256
+    assert f(*bufs, None, None, 200, 256, 256, 0, None, 0, None) == 2              # ragged M
+    assert f(MIS, *bufs[1:], None, None, 256, 256, 256, 0, None, 0, None) == 3      # misaligned A
+    assert f(*bufs, P(0x50008), P(0x60000), 256, 256, 256, 0, None, 0, None) == 3  # misaligned A8
+    assert f(*bufs, None, None, 1 << 30, 1 << 24, 128, 0, None, 0, None) == 2       # 2^37 tiles
+
+
+def test_ep_argument_checks(lib):
+    I64, I = ctypes.c_int64, ctypes.c_int
+    assert lib.fp8q_ep_row_bytes(7168) == 7168 + 224
+    assert lib.fp8q_ep_row_bytes(1024) == 1024 + 32
+    assert lib.fp8q_ep_row_bytes(128) == 128 + 16          # 4 bytes of scale, padded to 16
+    assert lib.fp8q_ep_row_bytes(100) == -1
+    r = lib.fp8q_ep_route
+    assert r(A16, 10, 2, 0, A16b, A16c, None) == 1           # no experts
+    assert r(A16, 10, 2, 257, A16b, A16c, None) == 2         # more than 256 experts
+    assert r(A16, 10, 0, 8, A16b, A16c, None) == 1           # k = 0
+    assert r(P(0x10002), 10, 2, 8, A16b, A16c, None) == 3    # misaligned ids
+    p = lib.fp8q_ep_pack
+    assert p(A16, A16b, A16c, 10, 2, 200, P(0x40000), None) == 2       # H % 128
+    assert p(MIS, A16b, A16c, 10, 2, 256, P(0x40000), None) == 3
+    assert p(None, None, None, 0, 2, 256, None, None) == 0             # no tokens: nothing to do
+    u = lib.fp8q_ep_unpack
+    args = (A16, 10, 256, A16b, A16c, 2, P(0x40000), P(0x50000), 2, P(0x60000), P(0x70000))
+    assert u(*args, 200, None) == 2                                     # Mp % 128
+    assert u(*args[:2], 200, *args[3:], 256, None) == 2                 # H % 128
+    c = lib.fp8q_ep_combine
+    assert c(A16, A16b, A16c, 4, 2, 12, P(0x40000), None) == 2         # N % 8
+    assert c(None, None, None, 0, 2, 16, None, None) == 0               # no tokens
+    g = lib.fp8q_ep_gather
+    assert g(A16, 256, 4, 12, A16b, A16c, 2, P(0x40000), None) == 2    # N % 8
