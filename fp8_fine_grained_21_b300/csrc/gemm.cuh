@@ -56,7 +56,7 @@ constexpr int kMaxGroups = 512;
 // quantizer: thread q converts row q of the A tile of each K block from BF16
 // to E4M3 (1x128 scale rule) straight into the operand stage, and the
 // promotion warpgroups move up by one.  Registers per lane then split
-// 32 (control) + 96 (quantizer) + 2 * 192 (promotion) = 512.
+// 40 (control) + 88 (quantizer) + 2 * 192 (promotion) = 512.
 template <int BN, bool kQA = false>
 struct GemmShape {
     static constexpr int kHalves = BN / 128;             // 128-column halves of the tile
@@ -67,8 +67,8 @@ struct GemmShape {
     static constexpr int kFirstPromoWarp = kQA ? 8 : 4;
     static constexpr int kThreads = 128 * (1 + kHalves + (kQA ? 1 : 0));
     static constexpr bool kRealloc = kHalves > 1;
-    static constexpr int kCtrlRegs = kQA ? 32 : 56;
-    static constexpr int kQuantRegs = 96;
+    static constexpr int kCtrlRegs = kQA ? 40 : 56;
+    static constexpr int kQuantRegs = 88;
     static constexpr int kPromoRegs = kQA ? 192 : 224;
     static constexpr int kLaunchRegs = (65536 / kThreads) & ~7;
     static_assert(!kRealloc || 128 * kCtrlRegs + (kQA ? 128 * kQuantRegs : 0) +
@@ -368,75 +368,44 @@ __device__ __forceinline__ void store_tile_tma(const float2* acc, uint8_t* stg,
     }
 }
 
-// In-kernel 1x128 quantization of the A tile (128 rows x 128 K) of one K
-// block, by the quantizer warpgroup.  Warp qw owns rows 32 qw .. 32 qw + 31
-// of the tile; it handles them in two halves of 16 rows, in 8 passes of two
-// rows each: in pass p of half hf, half-warp h (lanes 16h .. 16h + 15) holds
-// row 32 qw + 16 hf + 2p + h, lane l of it the 16-byte chunk of 8 BF16
-// values at columns 8 (l % 16) .. +7 -- so each load instruction reads two
-// whole 256-byte rows.  A half is loaded (qa_load_half) one half ahead of
-// its conversion (qa_convert_half), so the global loads overlap the
-// conversion of the previous half.
-__device__ __forceinline__ void qa_load_half(uint4 (&v)[8], const uint16_t* rows, int64_t K,
-                                             int kb, int hf, int lane) {
+// In-kernel 1x128 quantization of one row of one 128-K block: 128 BF16
+// values (v, 16 x 16 bytes) -> 128 E4M3 bytes written into the A tile of an
+// operand stage at row `row`, with the same 128-byte swizzle a TMA load of
+// the A8 tile would have produced (16-byte chunk j at j ^ (row % 8)).  The
+// scale rule is the quantizers': amax is exact (the largest BF16 magnitude,
+// found as the largest of the 15-bit magnitude fields, whose order equals the
+// order of the finite values), s = amax / 448 and inv = 448 / amax, both
+// correctly rounded, the cast is round-to-nearest-even and saturating.
+// Returns s.
+__device__ __forceinline__ float quant_row_to_stage(const uint4 (&v)[16], uint8_t* tile, int row) {
+    uint32_t m = 0;
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const int r = hf * 16 + 2 * p + (lane >> 4);           // row within the warp's 32
-        v[p] = __ldg(reinterpret_cast<const uint4*>(rows + r * K + kb * kBK + (lane & 15) * 8));
+    for (int i = 0; i < 16; ++i) {
+        m = __vmaxu2(m, v[i].x & 0x7FFF7FFFu);
+        m = __vmaxu2(m, v[i].y & 0x7FFF7FFFu);
+        m = __vmaxu2(m, v[i].z & 0x7FFF7FFFu);
+        m = __vmaxu2(m, v[i].w & 0x7FFF7FFFu);
     }
-}
-
-// Converts one half (16 rows) into the stage's A tile, with the 128-byte
-// swizzle a TMA load of the A8 tile would have produced (16-byte chunk j of
-// row r at j ^ (r % 8)), and stores the 16 rows' scales to slot[] (and
-// sa_out[], if given), both indexed by the row within the tile.  The scale
-// rule is the quantizers': amax is exact (the largest BF16 magnitude, found
-// as the largest 15-bit magnitude field, whose order equals that of the
-// finite values), s = amax / 448 and inv = 448 / amax are correctly rounded,
-// the cast rounds to nearest even and saturates.  Each row's maximum is
-// reduced over its half-warp; the 16 maxima are then gathered onto lanes
-// 0..15, which compute one row's scale each, and the inverses are
-// broadcast back.
-__device__ __forceinline__ void qa_convert_half(const uint4 (&v)[8], uint8_t* tile, float* slot,
-                                                float* sa_out, int qw, int hf, int lane) {
-    float mine = 0.0f;
+    const uint32_t mb = (m & 0xFFFFu) > (m >> 16) ? (m & 0xFFFFu) : (m >> 16);
+    float sc, inv;
+    group_scale(__uint_as_float(mb << 16), sc, inv);
+    uint8_t* base = tile + row * 128;
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        uint32_t m = __vmaxu2(__vmaxu2(v[p].x & 0x7FFF7FFFu, v[p].y & 0x7FFF7FFFu),
-                              __vmaxu2(v[p].z & 0x7FFF7FFFu, v[p].w & 0x7FFF7FFFu));
-        m = (m & 0xFFFFu) > (m >> 16) ? (m & 0xFFFFu) : (m >> 16);
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        const uint32_t t = __shfl_sync(0xffffffffu, m, (lane & 1) << 4);
-        if ((lane >> 1) == p) mine = __uint_as_float(t << 16);
-    }
-    float sc, inv_l;
-    group_scale(mine, sc, inv_l);                  // lane j < 16: row 16 hf + j of the warp
-    if (lane < 16) {
-        const int r = qw * 32 + hf * 16 + lane;
-        slot[r] = sc;
-        if (sa_out) sa_out[r] = sc;
-    }
+    for (int j = 0; j < 8; ++j) {          // 16 values per 16-byte chunk
+        const uint32_t w[8] = {v[2 * j].x, v[2 * j].y, v[2 * j].z, v[2 * j].w,
+                               v[2 * j + 1].x, v[2 * j + 1].y, v[2 * j + 1].z, v[2 * j + 1].w};
+        uint32_t o[4];
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const float inv = __shfl_sync(0xffffffffu, inv_l, 2 * p + (lane >> 4));
-        const int r = qw * 32 + hf * 16 + 2 * p + (lane >> 4);
-        const uint32_t w[4] = {v[p].x, v[p].y, v[p].z, v[p].w};
-        uint32_t o[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 4; ++h) {
             const uint32_t lo = cvt_e4m3x2(__fmul_rn(__uint_as_float(w[2 * h] << 16), inv),
                                            __fmul_rn(__uint_as_float(w[2 * h] & 0xFFFF0000u), inv));
             const uint32_t hi = cvt_e4m3x2(__fmul_rn(__uint_as_float(w[2 * h + 1] << 16), inv),
                                            __fmul_rn(__uint_as_float(w[2 * h + 1] & 0xFFFF0000u), inv));
             o[h] = lo | (hi << 16);
         }
-        const int li = lane & 15;
-        *reinterpret_cast<uint2*>(tile + r * 128 + ((((li >> 1) ^ (r & 7))) << 4) + (li & 1) * 8) =
-            make_uint2(o[0], o[1]);
+        *reinterpret_cast<uint4*>(base + ((j ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
+    return sc;
 }
 
 template <int BN, bool kRowB, bool kBf16Out, bool kQA = false>
@@ -612,16 +581,17 @@ __global__ void __launch_bounds__(GemmShape<BN, kQA>::kThreads, 1)
         }
     } else if (kQA && warp < S::kFirstPromoWarp) {
         // ----------------------------------------------------- quantizer
-        // Warp qw converts rows 32 qw .. 32 qw + 31 of every A tile into the
-        // operand stage (qa_convert_half), puts their scales in the slot ring
-        // for the promotion warps and, when the call emits the stored
-        // activations and this is the tile of column 0 (so that every block
-        // is emitted once), also into sA_out; lane 0 then copies the warp's
-        // 32 rows of E4M3 bytes out with a TMA store from the stage, whose
-        // layout is that of the A8 tensor map.  The next block's rows are
-        // loaded while the current one is converted.
+        // Thread q owns row q of every A tile: it loads the row's 128 BF16
+        // values of the block (before waiting for the stage, so the loads
+        // overlap the wait), quantizes them into the stage, puts the scale in
+        // the slot ring for the promotion warps, and -- when the call emits
+        // the stored activations and this is the tile of column 0, so that
+        // every block is emitted once -- writes the scale to sA_out; lane 0
+        // then copies the warp's 32 rows of E4M3 bytes out with a TMA store
+        // from the stage (its layout is that of the A8 tensor map).
         setmaxnreg_dec<S::kQuantRegs>();
-        const int qw = warp - S::kFirstQuantWarp;
+        const int q = threadIdx.x - S::kFirstQuantWarp * 32;
+        const int qw = q >> 5;
         uint32_t stage = 0, phase = 0, slot = 0, sphase = 0;
         bool ok = true;
         SegIter si;
@@ -631,14 +601,14 @@ __global__ void __launch_bounds__(GemmShape<BN, kQA>::kThreads, 1)
         while (ok && si.next(sg)) {
             const TileCoord tc = decode_tile<BN>(sg.t, grouped, N, args.G, gtile, grow);
             const bool emit = args.sA_out != nullptr && tc.n0 == 0;
-            const uint16_t* rows = args.Abf + static_cast<size_t>(tc.arow + qw * 32) * args.K;
-            uint4 va[8], vb[8];
-            qa_load_half(va, rows, args.K, sg.kb0, 0, lane);
-            qa_load_half(vb, rows, args.K, sg.kb0, 1, lane);
+            const uint16_t* src = args.Abf + static_cast<size_t>(tc.arow + q) * args.K;
 #pragma unroll 1
             for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1, args.status)) ||
-                    !__all_sync(0xffffffffu, mbar_wait(&sempty[slot], sphase ^ 1, args.status))) {
+                uint4 v[16];
+                const uint4* p = reinterpret_cast<const uint4*>(src + static_cast<size_t>(kb) * kBK);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __ldg(p + i);
+                if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1, args.status))) {
                     ok = false;
                     break;
                 }
@@ -648,13 +618,13 @@ __global__ void __launch_bounds__(GemmShape<BN, kQA>::kThreads, 1)
                 if (lane == 0) bulk_wait_read_pending<S::kStages - 1>();
                 __syncwarp();
                 uint8_t* tile = smem + stage * S::kStageBytes;
-                float* sl = reinterpret_cast<float*>(smem + S::kOffScale + slot * S::kSlotBytes);
-                float* so = emit ? args.sA_out + static_cast<size_t>(kb) * args.M_total + tc.arow
-                                 : nullptr;
-                qa_convert_half(va, tile, sl, so, qw, 0, lane);
-                if (kb + 1 < sg.kb1) qa_load_half(va, rows, args.K, kb + 1, 0, lane);
-                qa_convert_half(vb, tile, sl, so, qw, 1, lane);
-                if (kb + 1 < sg.kb1) qa_load_half(vb, rows, args.K, kb + 1, 1, lane);
+                const float sc = quant_row_to_stage(v, tile, q);
+                if (emit) args.sA_out[static_cast<size_t>(kb) * args.M_total + tc.arow + q] = sc;
+                if (!__all_sync(0xffffffffu, mbar_wait(&sempty[slot], sphase ^ 1, args.status))) {
+                    ok = false;
+                    break;
+                }
+                reinterpret_cast<float*>(smem + S::kOffScale + slot * S::kSlotBytes)[q] = sc;
                 fence_proxy_async_smem();          // the MMA reads the tile through the async proxy
                 __syncwarp();
                 if (lane == 0) {
