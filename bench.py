@@ -381,9 +381,13 @@ class L2Flush:
         self.r.sum()
 
 
-def time_graph(g, n, stream, flush):
-    """Mean device time of n replays, each preceded by an L2 flush that is
-    outside the events (and long enough to hide the host's enqueue time)."""
+def time_graph(g, n, stream, flush, median=False):
+    """Device time of n replays, each preceded by an L2 flush that is outside
+    the events (and long enough to hide the host's enqueue time): (mean, min,
+    mean), or (median, min, mean) with median=True.  Per-kernel figures use the median: a
+    replay whose launch reached the GPU late (a stall of the host thread
+    between the start event and the launch) is counted whole in its event
+    pair and would pull the mean of a ~20 us kernel far up."""
     evs = []
     for _ in range(n):
         flush()
@@ -395,7 +399,7 @@ def time_graph(g, n, stream, flush):
         evs.append((a, b))
     torch.cuda.synchronize()
     t = np.array([a.elapsed_time(b) for a, b in evs])
-    return float(t.mean()), float(t.min())
+    return float(np.median(t) if median else t.mean()), float(t.min()), float(t.mean())
 
 
 KERNEL_REPLAYS = 200             # per-kernel timing: replays, whatever --steps is
@@ -451,7 +455,7 @@ def time_quant_back_to_back(wl, stream, flush, reps=20):
                 fn(xi, qi, si, st)
 
         g = capture(run)
-        ms, _ = time_graph(g, reps, stream, flush)
+        ms, _, _ = time_graph(g, reps, stream, flush, median=True)
         out.append({"launches": R, "ms_per_launch": ms / R})
         del g, bufs
     return out
@@ -498,8 +502,8 @@ def dense_headline(fq, device, stream, flush):
         flush()
         g_step.replay()
     torch.cuda.synchronize()
-    step_ms, _ = time_graph(g_step, 50, stream, flush)
-    kt = [time_graph(g, KERNEL_REPLAYS, stream, flush) for g in g_parts]
+    step_ms, _, _ = time_graph(g_step, 50, stream, flush)
+    kt = [time_graph(g, KERNEL_REPLAYS, stream, flush, median=True) for g in g_parts]
     status = fq.fp8q_get_device_status()
     if status != 0:
         raise RuntimeError("device status after the dense headline: %s" % fq.fp8q_status_string(status))
@@ -654,13 +658,13 @@ def run_fp8q(args):
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
-    step_ms, step_min = time_graph(g_step, args.steps, stream, flush)
+    step_ms, step_min, _ = time_graph(g_step, args.steps, stream, flush)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     wall_ms = (time.perf_counter() - t_wall0) * 1e3
     # per-kernel device times (same flush discipline), for the roofline line
-    kt = [time_graph(g, KERNEL_REPLAYS, stream, flush) for g in g_parts]
+    kt = [time_graph(g, KERNEL_REPLAYS, stream, flush, median=True) for g in g_parts]
     q_b2b = time_quant_back_to_back(wl, stream, flush)
     clocks = sampler.stop()
     status = fq.fp8q_get_device_status()
@@ -670,8 +674,8 @@ def run_fp8q(args):
     if args.workload == "forward":
         # the same forward step with the activations quantized inside the GEMM
         g_fs, g_fg = capture(wl.fused_step), capture(wl.fused_gemm)
-        fs_ms, _ = time_graph(g_fs, KERNEL_REPLAYS, stream, flush)
-        fg_ms, _ = time_graph(g_fg, KERNEL_REPLAYS, stream, flush)
+        fs_ms, _, _ = time_graph(g_fs, KERNEL_REPLAYS, stream, flush)
+        fg_ms, _, _ = time_graph(g_fg, KERNEL_REPLAYS, stream, flush, median=True)
         fused = {"step_ms": fs_ms, "gemm_ms": fg_ms,
                  "step_tflops": wl.flops / (fs_ms * 1e-3) / 1e12,
                  "gemm_tflops": wl.flops / (fg_ms * 1e-3) / 1e12,
@@ -729,7 +733,8 @@ def run_fp8q(args):
             "frac_of_hbm": wl.quant_bytes[i] / (b["ms_per_launch"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
             for i, b in enumerate(q_b2b)],
         "kernel_ms": {"quant_a": kt[0][0], "quant_b": kt[1][0], "gemm": gemm_ms,
-                      "gemm_min": kt[2][1], "replays": KERNEL_REPLAYS},
+                      "gemm_min": kt[2][1], "gemm_mean": kt[2][2], "replays": KERNEL_REPLAYS,
+                      "statistic": "median"},
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
                      "traffic": profiled_traffic("gemm_" + args.workload),
