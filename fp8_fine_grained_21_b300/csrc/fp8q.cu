@@ -218,7 +218,7 @@ int encode_rows(CUtensorMap* map, const void* base, int in_dtype, int64_t cols, 
 template <typename Cfg, typename Kern>
 int launch_quant(DeviceState* d, bool& attr, Kern kern, const CUtensorMap& tm, int64_t tiles,
                  int64_t a, int64_t b, uint8_t* q, float* s, cudaStream_t st) {
-    constexpr int kSmem = Cfg::Ring::kSmemBytes;
+    constexpr int kSmem = Cfg::kSmemBytes;
     if (!attr) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
             cudaSuccess)
@@ -249,7 +249,25 @@ int quant_common(int kind, const void* x, int in_dtype, int64_t rows, int64_t co
                                     cols, q, s, st);
 }
 
-template <typename T> struct KQt { static constexpr auto fn = k_quant_128x1<T>; };
+// The 128x1 quantizer: its input map, plus the map of qT [C][T] (uint8) that
+// its TMA stores write, boxes of 128 tokens x 64 channels, 128-byte swizzle.
+template <typename T>
+int launch_quant_128x1(DeviceState* d, bool& attr, const CUtensorMap& tm, const CUtensorMap& tmq,
+                       int64_t tiles, int64_t T_, int64_t C, float* sT, cudaStream_t st) {
+    using Cfg = QtCfg<T>;
+    auto kern = k_quant_128x1<T>;
+    if (!attr) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::kSmemBytes) != cudaSuccess)
+            return cuda_fail();
+        attr = true;
+    }
+    int64_t grid = static_cast<int64_t>(d->num_sms) * Cfg::kCtasPerSm;
+    if (grid > tiles) grid = tiles;
+    kern<<<static_cast<unsigned>(grid), Cfg::kThreads, Cfg::kSmemBytes, st>>>(tm, tmq, T_, C, sT,
+                                                                              d->status);
+    return cudaGetLastError() == cudaSuccess ? FP8Q_OK : cuda_fail();
+}
 template <typename T> struct KQw { static constexpr auto fn = k_quant_128x128<T>; };
 
 template <int BN, bool kRowB, bool kBf16, bool kQA = false>
@@ -514,7 +532,16 @@ int fp8q_quant_act_128x1(const void* x, int in_dtype, int64_t T, int64_t C, uint
     if (T > kMaxTmaCoord || C > kMaxTmaCoord) return FP8Q_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(x, 16) || !aligned(qT, 16) || !aligned(sT, 4)) return FP8Q_ERR_MISALIGNED;
     const int64_t tiles = (C / 64) * (T / 128);
-    return quant_common<QtCfg, KQt>(0, x, in_dtype, T, C, 64, 128, tiles, qT, sT, stream);
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != FP8Q_OK) return rc;
+    CUtensorMap tm, tmq;
+    if ((rc = encode_rows(&tm, x, in_dtype, C, T, 64, 128)) != FP8Q_OK) return rc;
+    if ((rc = encode_kmajor(&tmq, qT, T, C, 64)) != FP8Q_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (in_dtype == FP8Q_BF16)
+        return launch_quant_128x1<__nv_bfloat16>(d, d->quant_attr[0][1], tm, tmq, tiles, T, C, sT, st);
+    return launch_quant_128x1<float>(d, d->quant_attr[0][0], tm, tmq, tiles, T, C, sT, st);
 }
 
 int fp8q_quant_w_128x128(const void* w, int in_dtype, int64_t N, int64_t K, uint8_t* q, float* s,

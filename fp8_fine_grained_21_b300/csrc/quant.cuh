@@ -437,6 +437,7 @@ struct QwCfg {
     static constexpr int kStages = sizeof(T) == 2 ? 3 : 2;
     static constexpr int kCtasPerSm = sizeof(T) == 2 ? 2 : 1;
     using Ring = TileRing<kStages, kTileBytes>;
+    static constexpr int kSmemBytes = Ring::kSmemBytes;
 };
 
 template <typename T>
@@ -505,27 +506,40 @@ __global__ void __launch_bounds__(256, QwCfg<T>::kCtasPerSm)
 // tokens of channel c from shared memory (conflict-free: a warp spans 32
 // consecutive channels of one token), the kParts partial maxima of a channel
 // meet in shared memory (double-buffered by iteration parity), and the
-// thread writes its kTok bytes of qT[c][t0 + kTok tp ..] (16-byte stores).
+// thread puts its kTok bytes of qT[c][t0 + kTok tp ..] into a staging tile of
+// 64 rows x 128 bytes laid out with the 128-byte swizzle (16-byte chunk j of
+// row r at j ^ (r % 8)).  One TMA store per tile writes the staged bytes:
+// per-thread stores of 32 bytes to 64 different rows of qT kept the
+// load-store unit's queue full (its throttle was the largest stall after the
+// loads).  The store of tile it is issued by thread 0 just after the CTA
+// barrier of tile it + 1 (which every thread reaches after staging tile it);
+// the staging tiles alternate, and before the barrier of tile it thread 0
+// waits until the store of tile it - 2, which read the same staging tile,
+// has read it.
 template <typename T>
 struct QtCfg {
     static constexpr int kThreads = 256;
     static constexpr int kParts = kThreads / 64;           // token ranges per channel
     static constexpr int kTok = 128 / kParts;              // tokens per thread
     static constexpr int kTileBytes = 128 * 64 * static_cast<int>(sizeof(T));
-    static constexpr int kStages = sizeof(T) == 2 ? 4 : 3;
+    static constexpr int kStages = sizeof(T) == 2 ? 3 : 2;
     static constexpr int kCtasPerSm = sizeof(T) == 2 ? 3 : 2;
     using Ring = TileRing<kStages, kTileBytes>;
+    static constexpr int kOutBytes = 64 * 128;              // one staged tile of qT
+    static constexpr int kOffOut = (Ring::kBarOffset + kStages * 8 + 1023) / 1024 * 1024;
+    static constexpr int kSmemBytes = kOffOut + 2 * kOutBytes + 1024;   // + alignment slack
 };
 
 template <typename T>
 __global__ void __launch_bounds__(QtCfg<T>::kThreads, QtCfg<T>::kCtasPerSm)
-    k_quant_128x1(const __grid_constant__ CUtensorMap tm, int64_t Tn, int64_t C,
-                  uint8_t* __restrict__ qT, float* __restrict__ sT, int* status) {
+    k_quant_128x1(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tmq,
+                  int64_t Tn, int64_t C, float* __restrict__ sT, int* status) {
     using Cf = QtCfg<T>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ float red[2][Cf::kParts][64];
     typename Cf::Ring ring;
     ring.init(smem_raw);
+    uint8_t* out = ring.base + Cf::kOffOut;        // two staged tiles of qT
     const int64_t CB = C / 64;
     const int64_t tiles = CB * (Tn / 128);
     const int n = my_tiles(tiles);
@@ -537,6 +551,7 @@ __global__ void __launch_bounds__(QtCfg<T>::kThreads, QtCfg<T>::kCtasPerSm)
             ring.load(j, &tm, static_cast<int32_t>((t % CB) * 64), static_cast<int32_t>((t / CB) * 128));
         }
     }
+    int32_t prev_x = 0, prev_y = 0;                // coordinates of the staged, unstored tile
 #pragma unroll 1
     for (int it = 0; it < n; ++it) {
         const int st = it % Cf::kStages;
@@ -554,15 +569,29 @@ __global__ void __launch_bounds__(QtCfg<T>::kThreads, QtCfg<T>::kCtasPerSm)
             }
             red[it & 1][tp][c] = a;
         }
+        // the staging tile about to be written was last read by the store of
+        // tile it - 2: that store must have read it before anyone writes
+        if (threadIdx.x == 0) bulk_wait_read_pending<0>();
         if (!__syncthreads_and(got)) {
-            if (threadIdx.x == 0) ring.drain(it, min(n - it, Cf::kStages));
+            if (threadIdx.x == 0) {
+                ring.drain(it, min(n - it, Cf::kStages));
+                bulk_wait_all();
+            }
             return;
         }
-        if (threadIdx.x == 0 && it + Cf::kStages < n) {
-            const int64_t tn = t + static_cast<int64_t>(Cf::kStages) * gridDim.x;
-            fence_proxy_async_smem();
-            ring.load(st, &tm, static_cast<int32_t>((tn % CB) * 64), static_cast<int32_t>((tn / CB) * 128));
+        if (threadIdx.x == 0) {
+            if (it > 0) {
+                tma_store_2d(&tmq, out + ((it - 1) & 1) * Cf::kOutBytes, prev_x, prev_y);
+                bulk_commit_group();
+            }
+            if (it + Cf::kStages < n) {
+                const int64_t tn = t + static_cast<int64_t>(Cf::kStages) * gridDim.x;
+                fence_proxy_async_smem();
+                ring.load(st, &tm, static_cast<int32_t>((tn % CB) * 64), static_cast<int32_t>((tn / CB) * 128));
+            }
         }
+        prev_x = static_cast<int32_t>(t0);
+        prev_y = static_cast<int32_t>(c0);
         float a = red[it & 1][0][c];
 #pragma unroll
         for (int p = 1; p < Cf::kParts; ++p) a = fmaxf(a, red[it & 1][p][c]);
@@ -576,10 +605,22 @@ __global__ void __launch_bounds__(QtCfg<T>::kThreads, QtCfg<T>::kCtasPerSm)
             const uint32_t hi = cvt_e4m3x2(__fmul_rn(v[4 * i + 2], inv), __fmul_rn(v[4 * i + 3], inv));
             w[i] = lo | (hi << 16);
         }
-        uint4* dst = reinterpret_cast<uint4*>(qT + (c0 + c) * Tn + t0 + tp * Cf::kTok);
+        uint8_t* row = out + (it & 1) * Cf::kOutBytes + c * 128;
 #pragma unroll
-        for (int i = 0; i < Cf::kTok / 16; ++i)
-            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        for (int i = 0; i < Cf::kTok / 16; ++i) {
+            const int chunk = tp * (Cf::kTok / 16) + i;           // 16-byte chunk of the row
+            *reinterpret_cast<uint4*>(row + ((chunk ^ (c & 7)) << 4)) =
+                make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+        fence_proxy_async_smem();                  // staged bytes -> the store's async read
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (n > 0) {
+            tma_store_2d(&tmq, out + ((n - 1) & 1) * Cf::kOutBytes, prev_x, prev_y);
+            bulk_commit_group();
+        }
+        bulk_wait_all();
     }
 }
 
