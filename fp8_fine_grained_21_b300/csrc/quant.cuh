@@ -678,9 +678,22 @@ __global__ void __launch_bounds__(256) k_retile_1x128_to_128x1(const uint8_t* __
         const uint32_t hi = cvt_e4m3x2(__fmul_rn(v[4 * i + 2], inv), __fmul_rn(v[4 * i + 3], inv));
         w[i] = lo | (hi << 16);
     }
-    uint4* dst = reinterpret_cast<uint4*>(qT + (c0 + c) * Tn + t0 + tp * 32);
-    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    // The input tile is free (every thread passed the barrier after its last
+    // read): stage the 64 channel rows x 128 token bytes there, 16-byte chunk
+    // j of row r at j ^ (r % 8), then write whole 128-byte rows of qT (a warp
+    // covers four rows) instead of 32 bytes into each of 64 rows per warp.
+    uint8_t* stg = &tile[0][0];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        *reinterpret_cast<uint4*>(stg + c * 128 + (((tp * 2 + i) ^ (c & 7)) << 4)) =
+            make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    __syncthreads();
+#pragma unroll
+    for (int id = threadIdx.x; id < 64 * 8; id += 256) {
+        const int r = id >> 3, j = id & 7;
+        *reinterpret_cast<uint4*>(qT + (c0 + r) * Tn + t0 + j * 16) =
+            *reinterpret_cast<const uint4*>(stg + r * 128 + ((j ^ (r & 7)) << 4));
+    }
 }
 
 // ------------------------------------------------- FP8 weight transpose
@@ -703,9 +716,14 @@ __global__ void __launch_bounds__(256) k_transpose_128x128(const uint8_t* __rest
     if (threadIdx.x == 0) sT[kb * (N / 128) + nb] = s[nb * (K / 128) + kb];
     __syncthreads();
     // output row k (a column of the block) gets 16 consecutive n per task;
-    // a warp's lanes take 32 consecutive k of the same n range
+    // a warp's lanes take 32 consecutive k of the same n range.  The 16-byte
+    // pieces are put back into the tile (row k, stride 144 bytes: a warp's
+    // stores spread over all banks) once every thread has read its columns,
+    // and leave as whole 128-byte rows of qT (a warp covers four rows).
+    uint4 wv[4];
 #pragma unroll
-    for (int id = threadIdx.x; id < 128 * 8; id += 256) {
+    for (int u = 0; u < 4; ++u) {
+        const int id = threadIdx.x + u * 256;
         const int k = id & 127, n0 = (id >> 7) * 16;
         uint32_t w[4];
 #pragma unroll
@@ -714,8 +732,21 @@ __global__ void __launch_bounds__(256) k_transpose_128x128(const uint8_t* __rest
                    (static_cast<uint32_t>(tile[n0 + 4 * i + 1][k]) << 8) |
                    (static_cast<uint32_t>(tile[n0 + 4 * i + 2][k]) << 16) |
                    (static_cast<uint32_t>(tile[n0 + 4 * i + 3][k]) << 24);
-        *reinterpret_cast<uint4*>(qT + (kb * 128 + k) * N + nb * 128 + n0) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        wv[u] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int id = threadIdx.x + u * 256;
+        const int k = id & 127, n0 = (id >> 7) * 16;
+        *reinterpret_cast<uint4*>(&tile[k][n0]) = wv[u];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int id = threadIdx.x; id < 128 * 8; id += 256) {
+        const int k = id >> 3, j = id & 7;
+        *reinterpret_cast<uint4*>(qT + (kb * 128 + k) * N + nb * 128 + j * 16) =
+            *reinterpret_cast<const uint4*>(&tile[k][j * 16]);
     }
 }
 
