@@ -187,6 +187,10 @@ class Workload:
             self.N = Bh.shape[0]
             self.inputs_host = [Ah, Bh]
             self.out_dtype = torch.bfloat16 if name == "forward" else torch.float32
+            if name == "accum":
+                # 32 tiles of 128 K blocks: the stream-K schedule cuts every tile,
+                # so the GEMM call adds the kernel that sums the pieces
+                self.launches_per_step = 4
         elif name == "wgrad":
             dY, X = d["dY"], d["X"]
             T, self.M = dY.shape

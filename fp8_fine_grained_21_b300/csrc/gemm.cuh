@@ -117,6 +117,9 @@ struct GemmArgs {
     const uint16_t* Abf;    // in-kernel quantization: BF16 activations [M_total][K]
     float* sA_out;          // in-kernel quantization: emitted 1x128 scales [K/128][M_total]
                             // (nullptr: none; A8 goes out through the tmA store map)
+    int sk_reduce;          // 1: stream-K pieces only write their partials; k_sk_reduce,
+                            // launched next, sums them (block-scaled B only); 0: the last
+                            // piece of each tile to arrive sums them in this kernel
 };
 
 // ------------------------------------------------------------ work schedule
@@ -134,7 +137,7 @@ struct Sched {
     int sk_ctas;            // CTAs 0 .. sk_ctas-1 share the stream-K iterations
     long long sk_iters;     // (tiles - dp_tiles) * Kb
 
-    __device__ void plan(int t_, int kb_, int g_, bool allow_sk) {
+    __host__ __device__ void plan(int t_, int kb_, int g_, bool allow_sk) {
         tiles = t_; Kb = kb_; G = g_;
         dp_tiles = tiles; sk_ctas = 0; sk_iters = 0;
         if (!allow_sk || tiles % G == 0) return;
@@ -153,17 +156,17 @@ struct Sched {
         if (sk_max + 16 >= dp_max) return;
         dp_tiles = dp; sk_ctas = static_cast<int>(g); sk_iters = S;
     }
-    __device__ long long lo(int c) const { return c < sk_ctas ? c * sk_iters / sk_ctas : 0; }
-    __device__ long long hi(int c) const { return c < sk_ctas ? (c + 1) * sk_iters / sk_ctas : 0; }
+    __host__ __device__ long long lo(int c) const { return c < sk_ctas ? c * sk_iters / sk_ctas : 0; }
+    __host__ __device__ long long hi(int c) const { return c < sk_ctas ? (c + 1) * sk_iters / sk_ctas : 0; }
     // CTA whose stream-K range holds iteration x.
-    __device__ int cta_of(long long x) const {
+    __host__ __device__ int cta_of(long long x) const {
         return static_cast<int>(((x + 1) * sk_ctas - 1) / sk_iters);
     }
     // Workspace slot of CTA c's piece of stream-K tile `rel`: each CTA has at
     // most two split pieces, the first (slot 2c) and the last (2c + 1) of its
     // range.  Of the CTAs c_lo..c_hi holding pieces of a tile, only c_lo's
     // piece can be the last of its range (its range starts before the tile).
-    __device__ int slot_in_tile(int c, int c_lo, bool clo_started_before) const {
+    __host__ __device__ int slot_in_tile(int c, int c_lo, bool clo_started_before) const {
         return 2 * c + ((c == c_lo && clo_started_before) ? 1 : 0);
     }
 };
@@ -179,10 +182,10 @@ struct SegIter {
     int c, t_dp;
     long long i, end;
     bool first;             // the next stream-K piece is the first of the range
-    __device__ void start(const Sched* s, int cta) {
+    __host__ __device__ void start(const Sched* s, int cta) {
         sc = s; c = cta; t_dp = cta; i = s->lo(cta); end = s->hi(cta); first = true;
     }
-    __device__ bool next(Seg& g) {
+    __host__ __device__ bool next(Seg& g) {
         if (t_dp < sc->dp_tiles) {
             g.t = t_dp; g.kb0 = 0; g.kb1 = sc->Kb; g.rel = -1;
             t_dp += sc->G;
@@ -752,6 +755,7 @@ __global__ void __launch_bounds__(GemmShape<BN, kQA>::kThreads, 1)
                 for (int j = 0; j < 32; ++j)
                     __stcg(mine + j * 32, make_float4(acc[2 * j].x, acc[2 * j].y, acc[2 * j + 1].x,
                                                       acc[2 * j + 1].y));
+                if (!kRowB && args.sk_reduce) continue;     // k_sk_reduce finishes the tile
                 __threadfence();
                 __syncwarp();
                 // pieces of this tile: one for each CTA c_lo .. c_hi
@@ -797,6 +801,71 @@ __global__ void __launch_bounds__(GemmShape<BN, kQA>::kThreads, 1)
         __syncwarp();
         tc_fence_before();
         cta_barrier(S::kThreads);
+    }
+}
+
+// ------------------------------------------------- stream-K reduction
+// The second kernel of a dense GEMM whose schedule cuts every tile (small
+// output, long K: no whole-tile wave runs beside the fix-up, so the in-kernel
+// sum by one CTA per tile -- ~600 KB of partials through 8 warps -- was half
+// the kernel's time).  CTA (rel, pw) sums slice pw (32 rows x 128 columns) of
+// stream-K tile rel over its pieces, in K order from zero -- the same
+// additions in the same order as the in-kernel fix-up -- and writes it to C.
+// A tile that one CTA's range covers whole was written by the GEMM itself.  Warp w takes the 16 columns of float4
+// groups 4w .. 4w + 3, lane l row l of the slice; the partial layout is the
+// GEMM's (slot, slice, float4 group, row), so each warp's reads are 512
+// contiguous bytes per group and every thread has its 20-odd loads in flight
+// at once (the in-kernel sum runs one CTA of 8 warps per tile).
+template <int BN, bool kBf16Out>
+__global__ void __launch_bounds__(256) k_sk_reduce(const float* __restrict__ ws, void* __restrict__ C,
+                                                   int N, Sched sc) {
+    constexpr int kPromoWarps = 4 * (BN / 128);
+    constexpr int kSliceF4 = 32 * 32;
+    const int rel = blockIdx.x, pw = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = sc.dp_tiles + rel;
+    const int ntn = N / BN;
+    const long long tile_start = static_cast<long long>(rel) * sc.Kb;
+    const int c_lo = sc.cta_of(tile_start);
+    const int c_hi = sc.cta_of(tile_start + sc.Kb - 1);
+    if (c_lo == c_hi) return;                       // one piece: written whole
+    const bool clo_before = sc.lo(c_lo) < tile_start;
+    float4 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 1
+    for (int c = c_lo; c <= c_hi; ++c) {
+        const float4* src = reinterpret_cast<const float4*>(ws) +
+                            (static_cast<size_t>(sc.slot_in_tile(c, c_lo, clo_before)) * kPromoWarps + pw) *
+                                kSliceF4 + warp * 4 * 32 + lane;
+        float4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = __ldcg(src + i * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[i].x += v[i].x;
+            acc[i].y += v[i].y;
+            acc[i].z += v[i].z;
+            acc[i].w += v[i].w;
+        }
+    }
+    const int half = pw >> 2, quarter = pw & 3;
+    const size_t row = static_cast<size_t>(t / ntn) * kBM + quarter * 32 + lane;
+    const int col = (t % ntn) * BN + half * 128 + warp * 16;
+    if (kBf16Out) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            w[2 * i] = pack_bf16x2(acc[i].x, acc[i].y);
+            w[2 * i + 1] = pack_bf16x2(acc[i].z, acc[i].w);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(C) + row * N + col);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    } else {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(C) + row * N + col);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = acc[i];
     }
 }
 

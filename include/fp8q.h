@@ -208,7 +208,10 @@ FP8Q_API int fp8q_gemm_grouped(const uint8_t* A8, const float* sA, const uint8_t
  * the last partial wave of output tiles (plus one full wave) out by K
  * iterations, so no SM idles at the end; tiles cut between SMs are finished
  * through FP32 partial tiles kept in the workspace.  Results do not depend on
- * the order in which the pieces finish.
+ * the order in which the pieces finish.  When the schedule cuts every tile of
+ * a dense GEMM with 128x128-block B scales (few tiles, long K), the call
+ * launches a second kernel after the GEMM, on the same stream, that sums the
+ * pieces; otherwise the last piece of each cut tile sums them.
  *
  * fp8q_gemm_workspace_size: bytes a workspace must have on the CURRENT device
  * (it depends on the SM count; about 38 MB on a 148-SM B300).  0 on error.
