@@ -265,8 +265,7 @@ FP8Q_API int fp8q_gemm_grouped_ws(const uint8_t* A8, const float* sA, const uint
                          size_t workspace_bytes, fp8q_stream_t stream);
 
 /* fp8q_gemm_ws without a caller workspace, for callers that cannot allocate
- * device memory: code that must not call cudaMalloc while a CUDA graph is
- * being captured, or that runs inside a framework or plugin whose memory is
+ * device memory: code that runs inside a framework or plugin whose memory is
  * handed out by someone else (a fixed budget, a caching allocator it cannot
  * reach), or that simply has no allocator of its own.  No counterpart on the
  * pages: this is an engineering convenience of the library, not part of the
