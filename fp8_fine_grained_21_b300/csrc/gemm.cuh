@@ -39,6 +39,8 @@ constexpr int kBM = 128;          // rows of A per tile (TMEM lanes)
 constexpr int kBK = 128;          // K per block = scale-group width = one 128-byte swizzle row
 constexpr int kScaleSlots = 8;
 constexpr int kScaleAhead = 4;    // block-scaled B: scale look-ahead of the promotion warps
+constexpr int kScaleRing = 8;     //   ring slots per promotion warp (more than kScaleAhead)
+constexpr int kRingSlotFloats = 36;   // 32 row scales + the block scale, padded to 16 bytes
 constexpr int kMaxGroups = 512;
 
 // Warp roles, by warpgroup (four consecutive warps, one on each SM
@@ -102,6 +104,8 @@ struct GemmShape {
     static constexpr int kOffGroups = kOffSched + 64;
     static constexpr int kSmemBytes = kOffGroups + 2 * (kMaxGroups + 1) * 4 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kPromoWarps * kScaleRing * kRingSlotFloats * 4 <= kScaleSlots * kSlotBytes,
+                  "the promotion warps' scale rings live in the slot area");
     static_assert(kTmemCols <= 512, "TMEM budget");
 };
 
@@ -660,29 +664,35 @@ __global__ void __launch_bounds__(GemmShape<BN, kQA>::kThreads, 1)
 #pragma unroll 1
         while (ok && si.next(sg)) {
             const TileCoord tc = decode_tile<BN>(sg.t, grouped, N, args.G, gtile, grow);
-            // Block-scaled B: this thread's row scale and the 128x128 block scale
-            // are read straight from global memory (coalesced) into a ring of
-            // kScaleAhead blocks: fa_q[0], fb_q[0] belong to block kb.  A load
-            // still in flight when the warp next waits costs that wait its
-            // remaining latency, so the ring is several blocks deep (measured:
-            // the forward GEMM 3% faster than with one block of look-ahead;
-            // eight blocks gain nothing over four).
-            const float* sa_row = args.sA + tc.arow + row;
+            // Block-scaled B: this warp's 32 row scales and its half's block
+            // scale of each K block come into the warp's own shared-memory ring
+            // by cp.async, kScaleAhead blocks ahead, and are read from there.
+            // A global load in flight in a promotion warp costs far more than
+            // its latency -- the warp's next barrier or TMEM wait waits for it
+            // (measured: the forward GEMM ~9% slower with the scales loaded by
+            // __ldg several blocks ahead than with none loaded) -- while
+            // cp.async writes no register and is waited for per thread.
             const float* sb_blk =
                 args.sB + (static_cast<size_t>(tc.e) * (N / 128) + (tc.n0 / 128 + half)) * Kb;
-            float fa_q[kScaleAhead], fb_q[kScaleAhead], fb_next = 0.0f;
+            float* sring = reinterpret_cast<float*>(smem + S::kOffScale) +
+                           pw * (kScaleRing * kRingSlotFloats);
+            const float* sa_lane = args.sA + tc.arow + quarter * 32 + lane;
+            // issue block k's copies (an empty group past the segment's end)
+            auto prefetch = [&](int k) {
+                if (k < sg.kb1) {
+                    float* sl = sring + (k % kScaleRing) * kRingSlotFloats;
+                    cp_async_4(sl + lane, sa_lane + static_cast<size_t>(k) * args.M_total);
+                    if (lane == 0) cp_async_4(sl + 32, sb_blk + k);
+                }
+                cp_async_commit();
+            };
+            float fb_next = 0.0f;
             if (kQA) {
                 fb_next = __ldg(sb_blk + sg.kb0);
             } else if (!kRowB) {
+                __syncwarp();                          // the last segment's reads are done
 #pragma unroll
-                for (int q = 0; q < kScaleAhead; ++q) {
-                    fa_q[q] = 0.0f;
-                    fb_q[q] = 0.0f;
-                    if (sg.kb0 + q < sg.kb1) {
-                        fa_q[q] = __ldg(sa_row + static_cast<size_t>(sg.kb0 + q) * args.M_total);
-                        fb_q[q] = __ldg(sb_blk + sg.kb0 + q);
-                    }
-                }
+                for (int q = 0; q < kScaleAhead; ++q) prefetch(sg.kb0 + q);
             }
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
@@ -701,18 +711,13 @@ __global__ void __launch_bounds__(GemmShape<BN, kQA>::kThreads, 1)
                     f = fa * fb_next;
                     if (kb + 1 < sg.kb1) fb_next = __ldg(sb_blk + kb + 1);
                 } else if (!kRowB) {
-                    fa = fa_q[0];
-                    f = fa_q[0] * fb_q[0];
-#pragma unroll
-                    for (int q = 0; q + 1 < kScaleAhead; ++q) {
-                        fa_q[q] = fa_q[q + 1];
-                        fb_q[q] = fb_q[q + 1];
-                    }
-                    if (kb + kScaleAhead < sg.kb1) {
-                        fa_q[kScaleAhead - 1] =
-                            __ldg(sa_row + static_cast<size_t>(kb + kScaleAhead) * args.M_total);
-                        fb_q[kScaleAhead - 1] = __ldg(sb_blk + kb + kScaleAhead);
-                    }
+                    cp_async_wait<kScaleAhead - 1>();  // this lane's copies for block kb
+                    __syncwarp();                      // and lane 0's block scale
+                    const float* sl = sring + (kb % kScaleRing) * kRingSlotFloats;
+                    fa = sl[lane];
+                    f = fa * sl[32];
+                    prefetch(kb + kScaleAhead);        // its slot was last read kScaleRing -
+                                                       // kScaleAhead blocks ago
                 } else {
                     if (!__all_sync(0xffffffffu, mbar_wait(&sfull[slot], sphase, args.status))) {
                         ok = false;
@@ -797,6 +802,7 @@ __global__ void __launch_bounds__(GemmShape<BN, kQA>::kThreads, 1)
             store_tile_tma<kBf16Out>(acc, smem + S::kOffEpi + pw * S::kEpiWarpBytes, &tmC,
                                      tc.n0 + half * 128, tc.arow + quarter * 32, lane);
         }
+        cp_async_wait<0>();                   // no scale copy still in flight
         if (lane == 0) bulk_wait_all();       // this warp's C stores have landed
         __syncwarp();
         tc_fence_before();
