@@ -11,17 +11,19 @@
 // WGMMA and promotion -- is prior art; this is its sm_103a counterpart):
 //   * producer warp (1 thread): TMA loads of the A tile (128 x 128 B) and
 //     B tile (BN x 128 B) into a ring of shared-memory stages (128-byte
-//     swizzle), plus bulk copies of the block's activation scales (and, for
-//     1x128-scaled B, the B scales) into a separate ring of scale slots;
+//     swizzle), plus, for 1x128-scaled B (weight gradient), bulk copies of
+//     both operands' scales of the block into a separate ring of scale slots;
 //   * MMA warp (1 thread): 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) per
-//     128-K block into one of two TMEM buffers (128 lanes x BN FP32
+//     128-K block into one of 512/BN TMEM buffers (128 lanes x BN FP32
 //     columns), a fresh accumulation per block; tcgen05.commit releases the
 //     smem stage and signals the promotion warps;
 //   * BN/128 promotion warpgroups: tcgen05.ld the partial in 16-column
 //     chunks (8 for row-scaled B), the next chunk's load in flight while the
 //     current one is scaled, release the TMEM buffer once the last chunk has
 //     arrived, and accumulate P * (sA * sB) into 128 FP32 registers per thread
-//     with packed FP32 FMAs; after the last block, write C.
+//     with packed FP32 FMAs (128x128-block B: each warp prefetches its scales
+//     into its own shared-memory ring with cp.async); after the last block,
+//     write C.
 // The MMA of block i+1 (other TMEM buffer) overlaps the promotion of block i.
 // Persistent: one CTA per SM walks tiles blockIdx.x, +gridDim.x, ...; the
 // rings carry over from one tile to the next.
